@@ -1,0 +1,183 @@
+/*
+ * ds4moe.h -- C ABI of the routed-MoE expert layer with 4-bit block-scaled
+ * experts (GB300 / sm_103a).
+ *
+ * The operation.  One routed mixture-of-experts feed-forward layer of the
+ * DwarfStar (ds4) engine, whose routed experts are stored in MXFP4 (gate, up
+ * and down projections) or, in the engine's asymmetric 2-bit scheme, with a
+ * Q2_K-style down projection ("DwarfStar実地分析: DeepSeek V4 Flashをローカルで
+ * 動かす狭域推論エンジン", §GGUFの対応範囲は意図的に狭い: only the routed experts
+ * are quantised, MXFP4 routed experts are used as published, Blackwell CUDA
+ * runs batched expert work on FP4 matrix instructions; "DS4 分布式Shell客户端",
+ * §模型下载: up/gate and down quantised asymmetrically, native MXFP4 experts).
+ * The pages give no formula; this library computes, per call on T tokens:
+ *
+ *   1. route    idx[t, 0..k) = the k largest router logits of token t, sorted
+ *               by (value desc, expert index asc); w[t, j] = softmax of those
+ *               k logits only.
+ *   2. group    the T*k (token, slot) pairs sorted by (expert, token).
+ *   3. gate/up  g = W_gate[e] x_t, u = W_up[e] x_t for every routed (t, e).
+ *   4. SwiGLU   h = g * sigmoid(g) * u.
+ *   5. down     y = W_down[e] h.
+ *   6. combine  out[t] = sum_j w[t, j] * y[t, j]   (fp32).
+ *
+ * Two execution paths compute it (chosen per call, see ds4moe_path_for):
+ *   DECODE  (T <= decode_max_tokens): weights streamed through registers,
+ *           activations kept at bf16/fp32 precision.
+ *   PREFILL (larger T): grouped block-scaled tcgen05 GEMMs; x and h are
+ *           quantised to MXFP8 (E4M3 + one E8M0 scale per 32 values, OCP MX
+ *           v1.0 conversion rule) inside the library; with a Q2_K down
+ *           projection h is kept in fp16 instead.
+ *
+ * Formats (OCP Microscaling Formats v1.0).  MXFP4 weight: 32 E2M1 codes along
+ * the contraction axis share one E8M0 scale byte (value 2^(b-127)); element
+ * 2i is the LOW nibble of byte i.  Q2_K-style super-block (256 weights along
+ * the contraction axis, 84 bytes): bytes 0..15 sub-block j scale byte (low
+ * nibble sc_j, high nibble m_j), bytes 16..79 2-bit q (weight i at byte
+ * 16 + i/4, bits 2*(i%4)), bytes 80..81 fp16 d, 82..83 fp16 dmin; weight =
+ * d*sc_j*q - dmin*m_j, j = i/16.
+ *
+ * Conventions for every call:
+ *   - Return value: DS4MOE_OK (0) or a negative DS4MOE_ERR_* code.  A call
+ *     that returns an error has enqueued no GPU work.
+ *   - "device pointer" = global memory of the layer's device; "host pointer"
+ *     = CPU memory (pinned memory gives the fastest copies).
+ *   - Every device pointer must be 16-byte aligned.
+ *   - Calls on one layer must not overlap: a layer owns its scratch buffers,
+ *     so use it from one stream at a time.
+ *   - NaN or infinite logits or activations are outside the layer's domain
+ *     (the output is then unspecified but the call is memory-safe).
+ */
+#ifndef DS4MOE_H
+#define DS4MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream).  NULL = legacy default stream. */
+typedef struct CUstream_st *ds4moe_stream_t;
+
+typedef struct ds4moe_layer ds4moe_layer; /* opaque, owned by the library */
+
+enum {
+    DS4MOE_OK = 0,
+    DS4MOE_ERR_INVALID_ARG = -1,      /* NULL/misaligned pointer, bad size, bad enum */
+    DS4MOE_ERR_UNSUPPORTED = -2,      /* shape the kernels do not cover, or no sm_103 device */
+    DS4MOE_ERR_CUDA = -3,             /* a CUDA runtime call failed */
+    DS4MOE_ERR_OOM = -4,              /* device allocation failed in create */
+    DS4MOE_ERR_TOO_MANY_TOKENS = -5,  /* T > config.max_tokens */
+    DS4MOE_ERR_DEVICE_TIMEOUT = -6    /* a kernel's bounded wait ran out (see get_status) */
+};
+
+enum { DS4MOE_DOWN_MXFP4 = 0, DS4MOE_DOWN_Q2K = 1 };
+enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2 };
+
+/* Layer shape and options.  Fill with ds4moe_config_default() first.
+ *   d_model    hidden size d; multiple of 128, 128..16384.
+ *   n_experts  routed experts E; 1..256.
+ *   d_ff       expert intermediate size f; multiple of 128 (MXFP4 down) or
+ *              of 256 (Q2_K down), 128..16384.
+ *   top_k      experts per token k; 1..min(8, E).
+ *   max_tokens largest T a forward call may pass (scratch is sized for it).
+ *   down_format      DS4MOE_DOWN_MXFP4 or DS4MOE_DOWN_Q2K.
+ *   decode_max_tokens  AUTO path choice: T <= this runs DECODE (default 64).
+ *   force_path       DS4MOE_PATH_* (AUTO by default; tests force a path).
+ *   debug_fault      0 in production.  1 = the first prefill GEMM drops one
+ *                    of its operand loads and its waits give up after ~1 ms,
+ *                    so ds4moe_get_status() reports DS4MOE_ERR_DEVICE_TIMEOUT
+ *                    (fault-handling test; the GPU stays usable).
+ *   wait_timeout_ms  bound on every device-side wait (default 2000). */
+typedef struct {
+    int32_t d_model, n_experts, d_ff, top_k;
+    int32_t max_tokens;
+    int32_t down_format;
+    int32_t decode_max_tokens;
+    int32_t force_path;
+    int32_t debug_fault;
+    int32_t wait_timeout_ms;
+} ds4moe_config;
+
+/* Canonical weight layout, DEVICE pointers, read only during create.
+ *   gate_codes, up_codes   uint8 [E][f][d/2]   MXFP4 codes, row = output unit
+ *   gate_scales, up_scales uint8 [E][f][d/32]  E8M0 scales
+ *   MXFP4 down: down_codes uint8 [E][d][f/2], down_scales uint8 [E][d][f/32]
+ *   Q2_K down:  down_codes uint8 [E][d][f/256][84], down_scales = NULL */
+typedef struct {
+    const uint8_t *gate_codes, *gate_scales;
+    const uint8_t *up_codes, *up_scales;
+    const uint8_t *down_codes, *down_scales;
+} ds4moe_weights;
+
+/* Fills *cfg with defaults (all shape fields 0; decode_max_tokens 64,
+ * wait_timeout_ms 2000, everything else 0). */
+void ds4moe_config_default(ds4moe_config *cfg);
+
+/* Validates cfg, allocates the layer on the CURRENT CUDA device, copies and
+ * repacks the weights into library-owned device memory, and synchronises the
+ * device before returning (so the caller may free its weight buffers).
+ * On success *out receives the layer; on failure *out is set to NULL and
+ * nothing stays allocated.  Errors: INVALID_ARG, UNSUPPORTED (shape or a
+ * device other than compute capability 10.3), OOM, CUDA. */
+int ds4moe_layer_create(const ds4moe_config *cfg, const ds4moe_weights *weights,
+                        ds4moe_layer **out);
+
+/* Enqueues one forward pass on `stream` and returns without synchronising.
+ *   x       device, bf16 [T][d] row-major (raw bits; 2 bytes per value)
+ *   logits  device, fp32 [T][E] row-major router logits
+ *   out     device, fp32 [T][d]; fully overwritten
+ *   T       0..max_tokens (T = 0 enqueues nothing)
+ * x, logits and out stay owned by the caller and must stay valid until the
+ * stream work completes; out must not alias x or logits.
+ * Errors (checked on the host before anything is enqueued): INVALID_ARG,
+ * TOO_MANY_TOKENS, CUDA (a launch failed).  Device-side timeouts surface
+ * later through ds4moe_get_status. */
+int ds4moe_forward(ds4moe_layer *layer, const void *x, const float *logits, float *out,
+                   int32_t T, ds4moe_stream_t stream);
+
+/* The same forward pass on HOST buffers: copies x and logits to
+ * library-owned device staging on `stream`, runs ds4moe_forward, copies out
+ * back, and synchronises `stream` before returning (out is then valid).
+ *   x host bf16 [T][d], logits host fp32 [T][E], out host fp32 [T][d].
+ * Errors: as ds4moe_forward, plus DEVICE_TIMEOUT if a kernel gave up. */
+int ds4moe_forward_host(ds4moe_layer *layer, const void *x, const float *logits, float *out,
+                        int32_t T, ds4moe_stream_t stream);
+
+/* Copies the routing of the most recent forward call (device-to-device, on
+ * `stream`) into caller buffers; any pointer may be NULL to skip it.
+ *   topk_idx  device int32 [T][k]   selected experts, best first
+ *   topk_w    device fp32  [T][k]   softmax weights
+ *   offsets   device int32 [E+1]    exclusive prefix sum of per-expert counts
+ *   perm_tok  device int32 [T*k]    token of each pair in (expert, token) order
+ * Errors: INVALID_ARG (no forward yet), CUDA. */
+int ds4moe_get_routing(ds4moe_layer *layer, int32_t *topk_idx, float *topk_w, int32_t *offsets,
+                       int32_t *perm_tok, ds4moe_stream_t stream);
+
+/* Synchronises the stream of the most recent forward, reads and clears the
+ * layer's device status word.  Returns DS4MOE_OK, DS4MOE_ERR_DEVICE_TIMEOUT
+ * (a bounded wait gave up; that forward's output is invalid) or
+ * DS4MOE_ERR_CUDA. */
+int ds4moe_get_status(ds4moe_layer *layer);
+
+/* DS4MOE_PATH_DECODE or DS4MOE_PATH_PREFILL for a call with T tokens, or a
+ * negative error for a NULL layer / T out of range. */
+int ds4moe_path_for(const ds4moe_layer *layer, int32_t T);
+
+/* Number of kernels one ds4moe_forward(T) enqueues (0 for T = 0), or a
+ * negative error. */
+int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
+
+/* Static, human-readable name of a status code. */
+const char *ds4moe_status_string(int status);
+
+/* Frees the layer and everything it owns.  NULL-safe.  The caller must have
+ * synchronised every stream the layer was used on. */
+void ds4moe_destroy(ds4moe_layer *layer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4MOE_H */

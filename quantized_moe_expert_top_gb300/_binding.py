@@ -1,0 +1,219 @@
+"""ctypes binding of libds4moe.so (include/ds4moe.h).
+
+Argument marshalling only: torch tensors supply device memory and
+``data_ptr()``; torch streams supply the ``cudaStream_t``.  Every step of the
+layer runs in the library's CUDA kernels; there is no Python or CPU fallback,
+and loading fails loudly when the compiled library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libds4moe.so")
+HEADER_PATH = os.path.join(_HERE, "..", "include", "ds4moe.h")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_CUDA = -3
+ERR_OOM = -4
+ERR_TOO_MANY_TOKENS = -5
+ERR_DEVICE_TIMEOUT = -6
+
+DOWN_MXFP4, DOWN_Q2K = 0, 1
+PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+_PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "prefill": PATH_PREFILL}
+_DOWN = {"mxfp4": DOWN_MXFP4, "q2k": DOWN_Q2K}
+
+
+class Ds4moeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "d_model", "n_experts", "d_ff", "top_k", "max_tokens", "down_format",
+        "decode_max_tokens", "force_path", "debug_fault", "wait_timeout_ms")]
+
+
+class WeightPtrs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales")]
+
+
+_lib = None
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/ds4moe.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"\b(ds4moe_[a-z_]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python quantized_moe_expert_top_gb300/build.py` (or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        L.ds4moe_config_default.restype = None
+        L.ds4moe_config_default.argtypes = [ctypes.POINTER(Config)]
+        L.ds4moe_layer_create.restype = ctypes.c_int
+        L.ds4moe_layer_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(WeightPtrs), ctypes.POINTER(vp)]
+        L.ds4moe_forward.restype = ctypes.c_int
+        L.ds4moe_forward.argtypes = [vp, vp, vp, vp, i32, vp]
+        L.ds4moe_forward_host.restype = ctypes.c_int
+        L.ds4moe_forward_host.argtypes = [vp, vp, vp, vp, i32, vp]
+        L.ds4moe_get_routing.restype = ctypes.c_int
+        L.ds4moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp]
+        L.ds4moe_get_status.restype = ctypes.c_int
+        L.ds4moe_get_status.argtypes = [vp]
+        L.ds4moe_path_for.restype = ctypes.c_int
+        L.ds4moe_path_for.argtypes = [vp, i32]
+        L.ds4moe_launches_per_forward.restype = ctypes.c_int
+        L.ds4moe_launches_per_forward.argtypes = [vp, i32]
+        L.ds4moe_status_string.restype = ctypes.c_char_p
+        L.ds4moe_status_string.argtypes = [ctypes.c_int]
+        L.ds4moe_destroy.restype = None
+        L.ds4moe_destroy.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().ds4moe_status_string(code).decode()
+
+
+def default_config() -> Config:
+    c = Config()
+    lib().ds4moe_config_default(ctypes.byref(c))
+    return c
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Layer:
+    """One routed-MoE expert layer owned by the library.
+
+    ``weights`` holds the canonical stored tensors on the current CUDA device
+    (uint8): gate_codes/up_codes [E,f,d/2], gate_scales/up_scales [E,f,d/32],
+    and either down_codes [E,d,f/2] + down_scales [E,d,f/32] (MXFP4) or
+    down_q2k [E,d,f/256,84] (Q2_K).  The library copies them; the caller may
+    free them after construction."""
+
+    def __init__(self, d_model: int, n_experts: int, d_ff: int, top_k: int, max_tokens: int,
+                 weights: dict, decode_max_tokens: int = 64, force_path: str = "auto",
+                 debug_fault: int = 0, wait_timeout_ms: int = 2000):
+        self._h = None
+        down = "q2k" if weights.get("down_q2k") is not None else "mxfp4"
+        c = default_config()
+        c.d_model, c.n_experts, c.d_ff, c.top_k = d_model, n_experts, d_ff, top_k
+        c.max_tokens = max_tokens
+        c.down_format = _DOWN[down]
+        c.decode_max_tokens = decode_max_tokens
+        c.force_path = _PATHS[force_path]
+        c.debug_fault = debug_fault
+        c.wait_timeout_ms = wait_timeout_ms
+        self.cfg = c
+        self.down = down
+        for name, t in weights.items():
+            if t is not None and (t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"weight {name} must be a contiguous uint8 CUDA tensor")
+        w = WeightPtrs()
+        w.gate_codes = weights["gate_codes"].data_ptr()
+        w.gate_scales = weights["gate_scales"].data_ptr()
+        w.up_codes = weights["up_codes"].data_ptr()
+        w.up_scales = weights["up_scales"].data_ptr()
+        if down == "q2k":
+            w.down_codes = weights["down_q2k"].data_ptr()
+            w.down_scales = None
+        else:
+            w.down_codes = weights["down_codes"].data_ptr()
+            w.down_scales = weights["down_scales"].data_ptr()
+        h = ctypes.c_void_p()
+        rc = lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h))
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_layer_create")
+        self._h = h
+        self._last_T = 0
+
+    # ------------------------------------------------------------------
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        """Enqueue one forward pass (asynchronous on `stream`)."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, device=x.device)
+        assert x.dtype == torch.bfloat16 and logits.dtype == torch.float32 and out.dtype == torch.float32
+        assert x.is_contiguous() and logits.is_contiguous() and out.is_contiguous()
+        rc = lib().ds4moe_forward(self._h, _ptr(x), _ptr(logits), _ptr(out), T, _stream_handle(stream))
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_forward")
+        self._last_T = T
+        return out
+
+    def forward_host(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+        """Forward pass on host tensors (copies in, runs, copies out, synchronises)."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, pin_memory=True)
+        assert not x.is_cuda and not logits.is_cuda and not out.is_cuda
+        rc = lib().ds4moe_forward_host(self._h, _ptr(x), _ptr(logits), _ptr(out), T, _stream_handle(stream))
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_forward_host")
+        self._last_T = T
+        return out
+
+    def routing(self, stream=None) -> dict:
+        """Routing tables of the last forward (device tensors)."""
+        T, k, E = self._last_T, self.cfg.top_k, self.cfg.n_experts
+        dev = torch.device("cuda", torch.cuda.current_device())
+        r = {"topk_idx": torch.empty(T, k, dtype=torch.int32, device=dev),
+             "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
+             "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+             "perm_tok": torch.empty(T * k, dtype=torch.int32, device=dev)}
+        rc = lib().ds4moe_get_routing(self._h, _ptr(r["topk_idx"]), _ptr(r["topk_w"]), _ptr(r["offsets"]),
+                                      _ptr(r["perm_tok"]), _stream_handle(stream))
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_get_routing")
+        return r
+
+    def status(self) -> int:
+        return lib().ds4moe_get_status(self._h)
+
+    def path_for(self, T: int) -> int:
+        return lib().ds4moe_path_for(self._h, T)
+
+    def launches_per_forward(self, T: int) -> int:
+        return lib().ds4moe_launches_per_forward(self._h, T)
+
+    def close(self):
+        if self._h is not None:
+            lib().ds4moe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

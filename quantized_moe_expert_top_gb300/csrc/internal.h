@@ -1,0 +1,106 @@
+// Internal declarations of the ds4moe library: the layer object, the device
+// buffers it owns, and the launchers of each kernel.  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4moe.h"
+
+namespace ds4moe {
+
+struct DeviceStatus;
+
+// Tile geometry of the prefill GEMMs.
+constexpr int kBM = 128;          // rows of a weight tile (tcgen05 M)
+constexpr int kBK = 128;          // contraction elements per pipeline stage
+constexpr int kPadRows = 128;     // each expert's token rows start on a 128-row boundary
+constexpr int kSfChunk = 512;     // bytes of one scale-factor chunk (128 rows x 4 blocks)
+constexpr int kGateUpNMax = 224;  // token columns per gate/up tile (two accumulators in TMEM)
+constexpr int kDownNMax = 256;    // token columns per down tile
+
+// Routing tables and scratch for one forward call (all device memory).
+struct Scratch {
+  int32_t* topk_idx;     // [Tmax*k]
+  float* topk_w;         // [Tmax*k]
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  int32_t* pad_offsets;  // [E+1] expert row starts in the 128-row padded order
+  int32_t* perm_tok;     // [Tmax*k]
+  int32_t* perm_slot;    // [Tmax*k]
+  int32_t* inv;          // [Tmax*k]  position of pair (t, j) in (expert, token) order
+  int32_t* pad_inv;      // [Tmax*k]  padded row of pair (t, j)
+  int32_t* pad_pair;     // [pad_rows_max] pair index t*k+j of a padded row (-1: padding)
+  int32_t* touched;      // [E+1] experts with at least one token, then their count at [E]
+  float* h_dec;          // [Tdec*k][f] decode-path SwiGLU output (fp32)
+  uint8_t* xq;           // [pad_rows_max][d]   MXFP8 codes of x, padded expert order
+  uint8_t* xsf;          // [pad_rows_max/128][d/128][512] E8M0 scales (tcgen05 chunk layout)
+  uint8_t* hq;           // [pad_rows_max][f]   MXFP8 codes of h (MXFP4 down)
+  uint8_t* hsf;          // [pad_rows_max/128][f/128][512]
+  __half* h16;           // [pad_rows_max][f]   fp16 h (Q2_K down)
+  uint8_t* stage_x;      // host-call staging: x [Tmax][d] bf16
+  float* stage_logits;   // [Tmax][E]
+  float* stage_out;      // [Tmax][d]
+  int64_t pad_rows_max;
+};
+
+// Weights as the kernels read them (library-owned device copies).
+struct Weights {
+  uint8_t *gate_codes, *up_codes;  // [E][f][d/2]  canonical MXFP4 codes
+  uint8_t *gate_scales, *up_scales;  // [E][f][d/32] canonical E8M0 (decode path)
+  uint8_t *gate_sf, *up_sf;          // [E][f/128][d/128][512] chunk layout (prefill)
+  uint8_t *down_codes, *down_scales, *down_sf;  // MXFP4 down: [E][d][f/2], [E][d][f/32], chunks
+  uint8_t* q2k_qs;     // Q2_K down: [E][d][f/4]   2-bit codes, 4 per byte
+  uint8_t* q2k_sc;     // [E][d][f/16]  sub-block scale bytes
+  uint32_t* q2k_dd;    // [E][d][f/256] (fp16 d | fp16 dmin << 16)
+};
+
+}  // namespace ds4moe
+
+struct ds4moe_layer {
+  ds4moe_config cfg;
+  int device;
+  int num_sms;
+  ds4moe::Weights w;
+  ds4moe::Scratch s;
+  ds4moe::DeviceStatus* status;  // device
+  // TMA descriptors (64-byte aligned inside the struct)
+  CUtensorMap tm_gate;  // 4-bit weights, box 128 x 128
+  CUtensorMap tm_up;
+  CUtensorMap tm_down;
+  CUtensorMap tm_xq;    // 8-bit activations, box 128 x 32
+  CUtensorMap tm_hq;
+  CUtensorMap tm_h16;   // fp16 h, box 64 x 32
+  int last_T;
+  cudaStream_t last_stream;
+  bool has_forward;
+  bool prefill_ready;  // tensor maps encoded
+  void* owned[48];     // every device allocation, freed by destroy
+  int n_owned;
+};
+
+namespace ds4moe {
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error; none synchronises.
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                              cudaStream_t st);
+cudaError_t launch_route_group(const ds4moe_layer* L, int T, cudaStream_t st);
+
+cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st);
+cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+
+cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st);
+cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, cudaStream_t st);
+cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+
+// create-time repacking
+cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, cudaStream_t st);
+cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream_t st);
+
+int decode_launches();
+int prefill_launches();
+
+}  // namespace ds4moe

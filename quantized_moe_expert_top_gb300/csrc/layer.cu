@@ -1,0 +1,448 @@
+// C ABI of the ds4moe library: layer creation (weight copies, repacking,
+// TMA descriptors), the forward planner, and the query calls.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace ds4moe;
+
+namespace {
+
+// Scale bytes [E][rows][K/32] (one per 32-element block) -> the chunk layout the
+// tensor-core scale copy reads: per (expert, 128-row block, 128-K block) one
+// 512-byte chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kblock % 4) for row r of
+// the block.
+__global__ void repack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int rows, int K) {
+  const int nkb = K / 32;
+  const size_t total = (size_t)E * rows * nkb;
+  const int MB = rows / kBM, KB = K / kBK;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int kb = (int)(i % nkb);
+    const size_t er = i / nkb;
+    const int r = (int)(er % rows);
+    const int e = (int)(er / rows);
+    const size_t chunk = ((size_t)e * MB + r / kBM) * KB + kb / 4;
+    const int rr = r % kBM;
+    dst[chunk * kSfChunk + (rr % 32) * 16 + (rr / 32) * 4 + (kb % 4)] = src[i];
+  }
+}
+
+// Q2_K super-blocks [E][d][f/256][84] -> split arrays with aligned rows:
+// qs [E][d][f/4], sc [E][d][f/16], dd [E][d][f/256] (d | dmin << 16).
+__global__ void repack_q2k_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ qs, uint8_t* __restrict__ sc,
+                                  uint32_t* __restrict__ dd, size_t nblocks) {
+  for (size_t b = (size_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += (size_t)gridDim.x * blockDim.x) {
+    const uint8_t* s = src + b * 84;
+    for (int i = 0; i < 16; ++i) sc[b * 16 + i] = s[i];
+    for (int i = 0; i < 64; ++i) qs[b * 64 + i] = s[16 + i];
+    dd[b] = (uint32_t)s[80] | ((uint32_t)s[81] << 8) | ((uint32_t)s[82] << 16) | ((uint32_t)s[83] << 24);
+  }
+}
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled get_encode_fn() {
+  static PFN_encodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_encodeTiled)p;
+  }
+  return fn;
+}
+
+// 2-D row-major tensor map: inner dimension `inner` elements, `rows` rows,
+// row pitch `pitch` bytes, box {box_inner, box_rows}, 128-byte swizzle.
+bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows, uint64_t pitch,
+               uint32_t box_inner, uint32_t box_rows) {
+  PFN_encodeTiled fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int validate_config(const ds4moe_config* c) {
+  if (!c) return DS4MOE_ERR_INVALID_ARG;
+  if (c->d_model < 128 || c->d_model > 8192 || c->d_model % 128) return DS4MOE_ERR_UNSUPPORTED;
+  if (c->d_ff < 128 || c->d_ff > 8192 || c->d_ff % 128) return DS4MOE_ERR_UNSUPPORTED;
+  if (c->n_experts < 1 || c->n_experts > 256) return DS4MOE_ERR_UNSUPPORTED;
+  if (c->top_k < 1 || c->top_k > 8 || c->top_k > c->n_experts) return DS4MOE_ERR_UNSUPPORTED;
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 20) / c->top_k) return DS4MOE_ERR_INVALID_ARG;
+  if (c->down_format != DS4MOE_DOWN_MXFP4 && c->down_format != DS4MOE_DOWN_Q2K) return DS4MOE_ERR_INVALID_ARG;
+  if (c->down_format == DS4MOE_DOWN_Q2K && c->d_ff % 256) return DS4MOE_ERR_UNSUPPORTED;
+  if (c->decode_max_tokens < 0) return DS4MOE_ERR_INVALID_ARG;
+  if (c->force_path < DS4MOE_PATH_AUTO || c->force_path > DS4MOE_PATH_PREFILL) return DS4MOE_ERR_INVALID_ARG;
+  if (c->wait_timeout_ms < 1 || c->wait_timeout_ms > 60000) return DS4MOE_ERR_INVALID_ARG;
+  return DS4MOE_OK;
+}
+
+template <typename Tp>
+int alloc(ds4moe_layer* L, Tp** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  if (L->n_owned >= (int)(sizeof(L->owned) / sizeof(L->owned[0]))) return DS4MOE_ERR_OOM;
+  void* q = nullptr;
+  if (cudaMalloc(&q, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_OOM;
+  }
+  L->owned[L->n_owned++] = q;
+  *p = static_cast<Tp*>(q);
+  return DS4MOE_OK;
+}
+
+int path_of(const ds4moe_layer* L, int T) {
+  if (L->cfg.down_format == DS4MOE_DOWN_Q2K) return DS4MOE_PATH_PREFILL;  // decode path streams MXFP4 only
+  if (L->cfg.force_path == DS4MOE_PATH_DECODE) return DS4MOE_PATH_DECODE;
+  if (L->cfg.force_path == DS4MOE_PATH_PREFILL) return DS4MOE_PATH_PREFILL;
+  return T <= L->cfg.decode_max_tokens ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
+}
+
+void free_all(ds4moe_layer* L) {
+  for (int i = 0; i < L->n_owned; ++i) cudaFree(L->owned[i]);
+  L->n_owned = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+void ds4moe_config_default(ds4moe_config* cfg) {
+  if (!cfg) return;
+  memset(cfg, 0, sizeof(*cfg));
+  cfg->decode_max_tokens = 64;
+  cfg->wait_timeout_ms = 2000;
+}
+
+const char* ds4moe_status_string(int s) {
+  switch (s) {
+    case DS4MOE_OK: return "ok";
+    case DS4MOE_ERR_INVALID_ARG: return "invalid argument";
+    case DS4MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case DS4MOE_ERR_CUDA: return "CUDA runtime error";
+    case DS4MOE_ERR_OOM: return "out of device memory";
+    case DS4MOE_ERR_TOO_MANY_TOKENS: return "T exceeds max_tokens";
+    case DS4MOE_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4moe_layer** out) {
+  if (!out) return DS4MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc != DS4MOE_OK) return rc;
+  if (!wts || !wts->gate_codes || !wts->gate_scales || !wts->up_codes || !wts->up_scales || !wts->down_codes)
+    return DS4MOE_ERR_INVALID_ARG;
+  if (cfg->down_format == DS4MOE_DOWN_MXFP4 && !wts->down_scales) return DS4MOE_ERR_INVALID_ARG;
+  if (!aligned16(wts->gate_codes) || !aligned16(wts->up_codes) || !aligned16(wts->down_codes))
+    return DS4MOE_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DS4MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DS4MOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return DS4MOE_ERR_UNSUPPORTED;
+
+  ds4moe_layer* L = new (std::nothrow) ds4moe_layer();
+  if (!L) return DS4MOE_ERR_OOM;
+  memset((void*)L, 0, sizeof(*L));
+  L->cfg = *cfg;
+  L->device = dev;
+  L->num_sms = prop.multiProcessorCount;
+
+  const int E = cfg->n_experts, d = cfg->d_model, f = cfg->d_ff, k = cfg->top_k, Tm = cfg->max_tokens;
+  const size_t gu_codes = (size_t)E * f * (d / 2), gu_scales = (size_t)E * f * (d / 32);
+  const size_t dn_codes = (size_t)E * d * (f / 2), dn_scales = (size_t)E * d * (f / 32);
+  const int64_t pairs = (int64_t)Tm * k;
+  const int64_t pad_rows = ((pairs + (int64_t)E * (kPadRows - 1)) + kPadRows - 1) / kPadRows * kPadRows;
+  const bool q2k = cfg->down_format == DS4MOE_DOWN_Q2K;
+  if (q2k && cfg->force_path == DS4MOE_PATH_DECODE) {  // the decode path streams MXFP4 rows only
+    delete L;
+    return DS4MOE_ERR_UNSUPPORTED;
+  }
+  const bool need_dec = !q2k && cfg->force_path != DS4MOE_PATH_PREFILL &&
+                        (cfg->force_path == DS4MOE_PATH_DECODE || cfg->decode_max_tokens > 0);
+  const bool need_pre = q2k || cfg->force_path == DS4MOE_PATH_PREFILL ||
+                        (cfg->force_path == DS4MOE_PATH_AUTO && Tm > cfg->decode_max_tokens);
+  const int Tdec = (cfg->force_path == DS4MOE_PATH_DECODE || Tm < cfg->decode_max_tokens) ? Tm
+                                                                                          : cfg->decode_max_tokens;
+  L->s.pad_rows_max = pad_rows;
+
+#define TRY(x)                 \
+  do {                         \
+    rc = (x);                  \
+    if (rc != DS4MOE_OK) goto fail; \
+  } while (0)
+  {
+    Weights& w = L->w;
+    Scratch& s = L->s;
+    TRY(alloc(L, &w.gate_codes, gu_codes));
+    TRY(alloc(L, &w.up_codes, gu_codes));
+    TRY(alloc(L, &w.gate_scales, gu_scales));
+    TRY(alloc(L, &w.up_scales, gu_scales));
+    if (need_pre) {
+      TRY(alloc(L, &w.gate_sf, gu_scales));
+      TRY(alloc(L, &w.up_sf, gu_scales));
+    }
+    if (!q2k) {
+      TRY(alloc(L, &w.down_codes, dn_codes));
+      TRY(alloc(L, &w.down_scales, dn_scales));
+      if (need_pre) TRY(alloc(L, &w.down_sf, dn_scales));
+    } else {
+      TRY(alloc(L, &w.q2k_qs, (size_t)E * d * (f / 4)));
+      TRY(alloc(L, &w.q2k_sc, (size_t)E * d * (f / 16)));
+      TRY(alloc(L, &w.q2k_dd, (size_t)E * d * (f / 256) * 4));
+    }
+    TRY(alloc(L, &s.topk_idx, pairs * 4));
+    TRY(alloc(L, &s.topk_w, pairs * 4));
+    TRY(alloc(L, &s.counts, (size_t)E * 4));
+    TRY(alloc(L, &s.offsets, (size_t)(E + 1) * 4));
+    TRY(alloc(L, &s.pad_offsets, (size_t)(E + 1) * 4));
+    TRY(alloc(L, &s.perm_tok, pairs * 4));
+    TRY(alloc(L, &s.perm_slot, pairs * 4));
+    TRY(alloc(L, &s.inv, pairs * 4));
+    TRY(alloc(L, &s.pad_inv, pairs * 4));
+    TRY(alloc(L, &s.pad_pair, (size_t)pad_rows * 4));
+    TRY(alloc(L, &s.touched, (size_t)(E + 1) * 4));
+    if (need_dec) TRY(alloc(L, &s.h_dec, (size_t)Tdec * k * f * 4));
+    if (need_pre) {
+      TRY(alloc(L, &s.xq, (size_t)pad_rows * d));
+      TRY(alloc(L, &s.xsf, (size_t)pad_rows * d / 32));
+      if (q2k) {
+        TRY(alloc(L, &s.h16, (size_t)pad_rows * f * 2));
+      } else {
+        TRY(alloc(L, &s.hq, (size_t)pad_rows * f));
+        TRY(alloc(L, &s.hsf, (size_t)pad_rows * f / 32));
+      }
+    }
+    TRY(alloc(L, &s.stage_x, (size_t)Tm * d * 2));
+    TRY(alloc(L, &s.stage_logits, (size_t)Tm * E * 4));
+    TRY(alloc(L, &s.stage_out, (size_t)Tm * d * 4));
+    TRY(alloc(L, &L->status, sizeof(DeviceStatus)));
+
+    cudaStream_t st = nullptr;
+    bool ok = cudaMemset(L->status, 0, sizeof(DeviceStatus)) == cudaSuccess;
+    ok = ok && cudaMemset(s.pad_pair, 0xFF, (size_t)pad_rows * 4) == cudaSuccess;
+    if (need_pre) {
+      // padding rows of the activation buffers hold zeros (finite codes)
+      ok = ok && cudaMemset(s.xq, 0, (size_t)pad_rows * d) == cudaSuccess;
+      ok = ok && cudaMemset(s.xsf, 127, (size_t)pad_rows * d / 32) == cudaSuccess;
+      if (q2k) {
+        ok = ok && cudaMemset(s.h16, 0, (size_t)pad_rows * f * 2) == cudaSuccess;
+      } else {
+        ok = ok && cudaMemset(s.hq, 0, (size_t)pad_rows * f) == cudaSuccess;
+        ok = ok && cudaMemset(s.hsf, 127, (size_t)pad_rows * f / 32) == cudaSuccess;
+      }
+    }
+    ok = ok && cudaMemcpy(w.gate_codes, wts->gate_codes, gu_codes, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(w.up_codes, wts->up_codes, gu_codes, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(w.gate_scales, wts->gate_scales, gu_scales, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(w.up_scales, wts->up_scales, gu_scales, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    if (!q2k) {
+      ok = ok && cudaMemcpy(w.down_codes, wts->down_codes, dn_codes, cudaMemcpyDeviceToDevice) == cudaSuccess;
+      ok = ok && cudaMemcpy(w.down_scales, wts->down_scales, dn_scales, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    }
+    if (!ok) {
+      rc = DS4MOE_ERR_CUDA;
+      goto fail;
+    }
+    if (need_pre) {
+      if (launch_repack_sf(w.gate_scales, w.gate_sf, E, f, d, st) != cudaSuccess ||
+          launch_repack_sf(w.up_scales, w.up_sf, E, f, d, st) != cudaSuccess ||
+          (!q2k && launch_repack_sf(w.down_scales, w.down_sf, E, d, f, st) != cudaSuccess)) {
+        rc = DS4MOE_ERR_CUDA;
+        goto fail;
+      }
+    }
+    if (q2k && launch_repack_q2k(wts->down_codes, L, st) != cudaSuccess) {
+      rc = DS4MOE_ERR_CUDA;
+      goto fail;
+    }
+    if (need_pre) {
+      bool tm_ok = encode_2d(&L->tm_gate, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gate_codes, d, (uint64_t)E * f,
+                             d / 2, 128, 128) &&
+                   encode_2d(&L->tm_up, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.up_codes, d, (uint64_t)E * f, d / 2,
+                             128, 128) &&
+                   encode_2d(&L->tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, 32);
+      if (!q2k) {
+        tm_ok = tm_ok &&
+                encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.down_codes, f, (uint64_t)E * d,
+                          f / 2, 128, 128) &&
+                encode_2d(&L->tm_hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, 32);
+      } else {
+        tm_ok = tm_ok && encode_2d(&L->tm_h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.h16, f, pad_rows, (uint64_t)f * 2,
+                                   64, 32);
+      }
+      if (!tm_ok) {
+        rc = DS4MOE_ERR_CUDA;
+        goto fail;
+      }
+      L->prefill_ready = true;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+      rc = DS4MOE_ERR_CUDA;
+      goto fail;
+    }
+  }
+#undef TRY
+  *out = L;
+  return DS4MOE_OK;
+fail:
+  cudaGetLastError();
+  free_all(L);
+  delete L;
+  return rc;
+}
+
+int ds4moe_path_for(const ds4moe_layer* L, int32_t T) {
+  if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > L->cfg.max_tokens) return DS4MOE_ERR_TOO_MANY_TOKENS;
+  return path_of(L, T);
+}
+
+int ds4moe_launches_per_forward(const ds4moe_layer* L, int32_t T) {
+  const int p = ds4moe_path_for(L, T);
+  if (p < 0) return p;
+  if (T == 0) return 0;
+  return p == DS4MOE_PATH_DECODE ? decode_launches() : prefill_launches();
+}
+
+int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
+                   ds4moe_stream_t stream) {
+  if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (T < 0) return DS4MOE_ERR_INVALID_ARG;
+  if (T > L->cfg.max_tokens) return DS4MOE_ERR_TOO_MANY_TOKENS;
+  if (T == 0) return DS4MOE_OK;
+  if (!x || !logits || !out || !aligned16(x) || !aligned16(logits) || !aligned16(out)) return DS4MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int path = path_of(L, T);
+  if (path == DS4MOE_PATH_DECODE && !L->s.h_dec) return DS4MOE_ERR_UNSUPPORTED;
+  if (path == DS4MOE_PATH_PREFILL && !L->prefill_ready) return DS4MOE_ERR_UNSUPPORTED;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != L->device) return DS4MOE_ERR_INVALID_ARG;
+
+  L->last_stream = st;
+  cudaError_t e = launch_route_topk(logits, T, L->cfg.n_experts, L->cfg.top_k, L->s.topk_idx, L->s.topk_w, st);
+  if (e == cudaSuccess) e = launch_route_group(L, T, st);
+  if (path == DS4MOE_PATH_DECODE) {
+    if (e == cudaSuccess) e = launch_decode_gateup(L, x, out, T, st);
+    if (e == cudaSuccess) e = launch_decode_down(L, out, T, st);
+  } else {
+    if (e == cudaSuccess) e = launch_act_quant(L, x, out, T, st);
+    if (e == cudaSuccess) e = launch_gemm_gateup(L, T, st);
+    if (e == cudaSuccess) {
+      if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = launch_gemm_down_q2k(L, out, T, st);
+      else e = launch_gemm_down(L, out, T, st);
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  L->last_T = T;
+  L->has_forward = true;
+  return DS4MOE_OK;
+}
+
+int ds4moe_forward_host(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
+                        ds4moe_stream_t stream) {
+  if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (T < 0) return DS4MOE_ERR_INVALID_ARG;
+  if (T > L->cfg.max_tokens) return DS4MOE_ERR_TOO_MANY_TOKENS;
+  if (T == 0) return DS4MOE_OK;
+  if (!x || !logits || !out) return DS4MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * L->cfg.d_model * 2, lb = (size_t)T * L->cfg.n_experts * 4,
+               ob = (size_t)T * L->cfg.d_model * 4;
+  if (cudaMemcpyAsync(L->s.stage_x, x, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(L->s.stage_logits, logits, lb, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  int rc = ds4moe_forward(L, L->s.stage_x, L->s.stage_logits, L->s.stage_out, T, stream);
+  if (rc != DS4MOE_OK) return rc;
+  if (cudaMemcpyAsync(out, L->s.stage_out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  return ds4moe_get_status(L);  // synchronises the stream, reads and clears the status word
+}
+
+int ds4moe_get_routing(ds4moe_layer* L, int32_t* topk_idx, float* topk_w, int32_t* offsets, int32_t* perm_tok,
+                       ds4moe_stream_t stream) {
+  if (!L || !L->has_forward) return DS4MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t pairs = (size_t)L->last_T * L->cfg.top_k;
+  bool ok = true;
+  if (topk_idx) ok = ok && cudaMemcpyAsync(topk_idx, L->s.topk_idx, pairs * 4, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+  if (topk_w) ok = ok && cudaMemcpyAsync(topk_w, L->s.topk_w, pairs * 4, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+  if (offsets)
+    ok = ok && cudaMemcpyAsync(offsets, L->s.offsets, (size_t)(L->cfg.n_experts + 1) * 4, cudaMemcpyDeviceToDevice,
+                               st) == cudaSuccess;
+  if (perm_tok) ok = ok && cudaMemcpyAsync(perm_tok, L->s.perm_tok, pairs * 4, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  return DS4MOE_OK;
+}
+
+int ds4moe_get_status(ds4moe_layer* L) {
+  if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (L->has_forward && cudaStreamSynchronize(L->last_stream) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  DeviceStatus hs;
+  if (cudaMemcpy(&hs, L->status, sizeof(hs), cudaMemcpyDeviceToHost) != cudaSuccess) return DS4MOE_ERR_CUDA;
+  if (hs.code != kStatusOk) {
+    DeviceStatus z;
+    memset(&z, 0, sizeof(z));
+    if (cudaMemcpy(L->status, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return DS4MOE_ERR_CUDA;
+    return DS4MOE_ERR_DEVICE_TIMEOUT;
+  }
+  return DS4MOE_OK;
+}
+
+void ds4moe_destroy(ds4moe_layer* L) {
+  if (!L) return;
+  free_all(L);
+  delete L;
+}
+
+}  // extern "C"
+
+namespace ds4moe {
+
+cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, cudaStream_t st) {
+  const size_t total = (size_t)E * rows * (K / 32);
+  const int blocks = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
+  repack_sf_kernel<<<blocks, 256, 0, st>>>(scales, sf, E, rows, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream_t st) {
+  const size_t nb = (size_t)L->cfg.n_experts * L->cfg.d_model * (L->cfg.d_ff / 256);
+  const int grid = (int)((nb + 255) / 256 < 65536 ? (nb + 255) / 256 : 65536);
+  repack_q2k_kernel<<<grid, 256, 0, st>>>(blocks, L->w.q2k_qs, L->w.q2k_sc, L->w.q2k_dd, nb);
+  return cudaGetLastError();
+}
+
+}  // namespace ds4moe

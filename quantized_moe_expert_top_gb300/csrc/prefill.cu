@@ -1,0 +1,518 @@
+// Prefill (many-token) path of the routed-MoE layer: grouped block-scaled
+// GEMMs on the 5th-generation tensor cores.
+//
+// "DwarfStar実地分析" §GGUFの対応範囲は意図的に狭い states that on Blackwell CUDA
+// the batched expert work runs on FP4 matrix instructions.  Here every expert's
+// tokens form one GEMM with the weights as the M side (swap-AB: 128 weight rows
+// per tile, the expert's tokens as N, so a ragged token count only pads N to 16):
+//
+//   gate/up : tcgen05.mma kind::mxf8f6f4 block_scale, A = E2M1 weights (TMA
+//             expands the packed nibbles into the 16-byte-aligned layout the
+//             MMA reads), B = E4M3 activations, one E8M0 scale per 32 K for
+//             both, fp32 accumulators in tensor memory.  Gate and up rows go
+//             to two accumulators, so the epilogue has g and u of the same
+//             (unit, token) in one thread: it applies SwiGLU and quantises h
+//             to MXFP8 along f (or to fp16 for the Q2_K down projection).
+//   down    : same MMA on h; the epilogue multiplies by the routing weight and
+//             red-adds into out[t] (the weighted combine back to token order).
+//
+// Warp roles per CTA (persistent, one CTA per SM): warp 0 issues TMA loads,
+// warp 1 allocates tensor memory and issues MMAs, warps 2..5 drain the
+// accumulators.  Every mbarrier wait is bounded; a wait that runs out records
+// DS4MOE_ERR_DEVICE_TIMEOUT in the layer's status word, the CTA drains its
+// in-flight copies and MMAs (again bounded), frees its tensor memory and exits.
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds4moe {
+namespace {
+
+// --------------------------------------------------------------- MXFP8 of x
+// One warp per token.  Lane l quantises blocks l, l+32, ... of x[t] (32 bf16
+// each) to E4M3 with one E8M0 scale (s = floor(log2 amax) - 8, clamped; 0 for
+// an all-zero block), then writes the codes and the scale to the k padded rows
+// of the token's routed pairs.  Also zeroes out[t] for the down epilogue.
+__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k,
+                                                        const int32_t* __restrict__ pad_inv, uint8_t* __restrict__ xq,
+                                                        uint8_t* __restrict__ xsf, float* __restrict__ out) {
+  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  {
+    float4* o = reinterpret_cast<float4*>(out + (size_t)t * d);
+    for (int i = lane; i < d / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  int rows[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(pad_inv + (size_t)t * k + j) : 0;
+  const int nblk = d / 32, kgs = d / 128;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+  for (int c = lane; c < nblk; c += 32) {
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(src + 4 * c + q);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v[8 * q + 2 * h] = __uint_as_float(wv[h] << 16);
+        v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    int s = 0;
+    if (amax > 0.f) s = max(-127, min(127, floor_log2_f32(amax) - 8));
+    const float inv = exp2i(-s);
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
+      const uint32_t hi = f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+      packed[i] = lo | (hi << 16);
+    }
+    const uint4 c0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    const uint4 c1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    const uint8_t sb = (uint8_t)(s + 127);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const size_t r = (size_t)rows[j];
+        uint4* dst = reinterpret_cast<uint4*>(xq + r * d + 32 * (size_t)c);
+        dst[0] = c0;
+        dst[1] = c1;
+        xsf[((r / 128) * kgs + c / 4) * kSfChunk + (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4)] = sb;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------- GEMM
+enum class Mode { GateUp, Down };
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A/B formats
+// (E4M3 = 0, E2M1 = 5), K-major A and B, N >> 3, E8M0 scales, M >> 4, and the
+// byte of the 32-bit scale word (one per 32-K step) used for A and B.
+__device__ __forceinline__ uint32_t idesc_mx(int N, uint32_t sf_id) {
+  constexpr uint32_t kE2M1 = 5, kE4M3 = 0;
+  return (sf_id << 4) | (kE2M1 << 7) | (kE4M3 << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(kBM >> 4) << 24) | (sf_id << 29);
+}
+
+template <Mode M>
+struct Cfg;
+template <>
+struct Cfg<Mode::GateUp> {
+  static constexpr int kNumA = 2;
+  static constexpr int kNMax = 192;
+  static constexpr int kStages = 3;
+  static constexpr int kAccCol2 = 256;  // up accumulator column
+  static constexpr int kSfBase = 448;   // scale-factor slots (16 columns each)
+  static constexpr int kSfSlot = 16;
+  static constexpr int kSfSlots = 4;
+};
+template <>
+struct Cfg<Mode::Down> {
+  static constexpr int kNumA = 1;
+  static constexpr int kNMax = 256;
+  static constexpr int kStages = 4;
+  static constexpr int kAccCol2 = 0;
+  static constexpr int kSfBase = 256;
+  static constexpr int kSfSlot = 12;
+  static constexpr int kSfSlots = 4;
+};
+
+static_assert(Cfg<Mode::GateUp>::kSfSlots >= Cfg<Mode::GateUp>::kStages, "scale slots");
+static_assert(Cfg<Mode::Down>::kSfSlots >= Cfg<Mode::Down>::kStages, "scale slots");
+
+template <Mode M>
+struct Smem {
+  static constexpr int kA = kBM * kBK;                    // 16 KB per weight tile
+  static constexpr int kB = Cfg<M>::kNMax * kBK;           // token tile
+  static constexpr int kSf = (kSfChunk * (Cfg<M>::kNumA + 2) + 1023) / 1024 * 1024;
+  static constexpr int kStage = Cfg<M>::kNumA * kA + kB + kSf;
+  static constexpr int kBarOff = Cfg<M>::kStages * kStage;
+  static constexpr int kTotal = kBarOff + 256 + 1024;     // + barriers, + alignment slack
+};
+static_assert(Smem<Mode::GateUp>::kStage % 1024 == 0, "stage alignment");
+static_assert(Smem<Mode::Down>::kStage % 1024 == 0, "stage alignment");
+
+struct GemmArgs {
+  // weights
+  const uint8_t* sfa0;  // chunk-layout scales of A0 (gate or down)
+  const uint8_t* sfa1;  // up
+  int rows_per_expert;  // f (gate/up) or d (down)
+  int K;                // d (gate/up) or f (down)
+  // activations (B)
+  const uint8_t* sfb;   // chunk-layout scales of the B rows
+  // routing
+  const int32_t* counts;
+  const int32_t* pad_offsets;
+  const int32_t* pad_pair;
+  const float* topk_w;
+  int E, k, d, f;
+  // outputs
+  uint8_t* hq;    // gate/up: MXFP8 h codes [rows][f]
+  uint8_t* hsf;   // gate/up: h scales (chunk layout)
+  __half* h16;    // gate/up: fp16 h (Q2_K down), or nullptr
+  float* out;     // down: [T][d]
+  DeviceStatus* status;
+  uint64_t budget_ns;
+  int debug_fault;
+};
+
+// Work unit sequence shared by the three roles: units u = (expert, 128-row
+// block), expert-major; each unit's tokens split into chunks that start on a
+// 128-token boundary (one chunk when they fit in kNMax columns).
+struct UnitIter {
+  int u, nunits, stride, mb_per_e;
+  int e, mb, ne, t0, nch;
+  const int32_t* counts;
+  int nmax;
+  __device__ bool first_chunk() {
+    for (; u < nunits; u += stride) {
+      e = u / mb_per_e;
+      mb = u % mb_per_e;
+      ne = __ldg(counts + e);
+      if (ne > 0) {
+        t0 = 0;
+        nch = ne <= nmax ? ne : 128;
+        return true;
+      }
+    }
+    return false;
+  }
+  __device__ bool next() {
+    t0 += nch;
+    if (t0 < ne) {
+      const int rem = ne - t0;
+      nch = rem <= nmax ? rem : 128;
+      return true;
+    }
+    u += stride;
+    return first_chunk();
+  }
+};
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+template <Mode M>
+__global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                                                              const __grid_constant__ CUtensorMap tm_a1,
+                                                              const __grid_constant__ CUtensorMap tm_b,
+                                                              const GemmArgs args) {
+  using C = Cfg<M>;
+  using S = Smem<M>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mb_per_e = args.rows_per_expert / kBM;
+  const int nunits = args.E * mb_per_e;
+  const int KB = args.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_a0);
+    if (C::kNumA > 1) prefetch_tmap(&tm_a1);
+    prefetch_tmap(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true, fault_pending = args.debug_fault && blockIdx.x == 0;
+      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
+        const int N = round16(it.nch);
+        const int nb = (N + 31) / 32, nsf = (N + 127) / 128;
+        const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+        const int arow = it.e * args.rows_per_expert + it.mb * kBM;
+        const uint32_t bytes = (uint32_t)(C::kNumA * S::kA + nb * 32 * kBK + (C::kNumA + nsf) * kSfChunk);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
+            report_timeout(args.status, kWhereProducerEmpty);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * S::kStage;
+          uint8_t* sa0 = st;
+          uint8_t* sa1 = st + S::kA;
+          uint8_t* sb = st + C::kNumA * S::kA;
+          uint8_t* ssf = sb + S::kB;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          if (fault_pending) {
+            fault_pending = false;  // test-only: drop this stage's loads
+          } else {
+            tma_load_2d(sa0, &tm_a0, &full[stage], kb * kBK, arow);
+            if (C::kNumA > 1) tma_load_2d(sa1, &tm_a1, &full[stage], kb * kBK, arow);
+            for (int i = 0; i < nb; ++i) tma_load_2d(sb + i * 32 * kBK, &tm_b, &full[stage], kb * kBK, prow + 32 * i);
+            const size_t sfa_off = ((size_t)(it.e * mb_per_e + it.mb) * KB + kb) * kSfChunk;
+            bulk_load(ssf, args.sfa0 + sfa_off, kSfChunk, &full[stage]);
+            if (C::kNumA > 1) bulk_load(ssf + kSfChunk, args.sfa1 + sfa_off, kSfChunk, &full[stage]);
+            for (int i = 0; i < nsf; ++i)
+              bulk_load(ssf + (C::kNumA + i) * kSfChunk, args.sfb + ((size_t)(prow / 128 + i) * KB + kb) * kSfChunk,
+                        kSfChunk, &full[stage]);
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: every issued stage's copies must land before the CTA exits
+        for (int s = 0; s < C::kStages; ++s)
+          if ((issued_mask >> s) & 1u) {
+            volatile int never = 0;
+            mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, args.budget_ns, &never);
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      uint32_t sf_seq = 0;  // running stage count; slot = sf_seq % kSfSlots (kSfSlots >= kStages)
+      bool ok = true;
+      const uint32_t sf_tmem = tmem + C::kSfBase;
+      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
+        const int N = round16(it.nch);
+        const int nsf = (N + 127) / 128;
+        if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, args.budget_ns, abort_flag)) {
+          report_timeout(args.status, kWhereMmaAccEmpty);
+          *abort_flag = 1;
+          break;
+        }
+        acc_phase ^= 1u;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag)) {
+            report_timeout(args.status, kWhereMmaFull);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* st = smem + stage * S::kStage;
+          const uint32_t a0 = smem_u32(st), a1 = smem_u32(st + S::kA);
+          const uint32_t b = smem_u32(st + C::kNumA * S::kA);
+          const uint32_t ssf = b + S::kB;
+          const uint32_t slot = sf_tmem + (sf_seq++ % C::kSfSlots) * C::kSfSlot;
+          // scale factors -> tensor memory: A chunk(s) at slot+0 (+4), B chunks after
+          for (int i = 0; i < C::kNumA + nsf; ++i)
+            tc_cp_32x128b_warpx4(slot + 4 * i, smem_desc(ssf + i * kSfChunk, 0, 128, 0));
+#pragma unroll
+          for (int j = 0; j < kBK / 32; ++j) {
+            const uint32_t idesc = idesc_mx(N, (uint32_t)j);
+            const uint64_t bd = smem_desc(b + 32 * j, 16, 1024, 2);
+            const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+            mma_mxf8f6f4(tmem, smem_desc(a0 + 32 * j, 16, 1024, 2), bd, idesc, slot, slot + 4 * C::kNumA, accum);
+            if (C::kNumA > 1)
+              mma_mxf8f6f4(tmem + C::kAccCol2, smem_desc(a1 + 32 * j, 16, 1024, 2), bd, idesc, slot + 4,
+                           slot + 4 * C::kNumA, accum);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+      // drain all MMAs this thread issued before tensor memory is freed
+      tc_commit(drain);
+      volatile int never = 0;
+      mbar_wait_bounded(drain, 0, args.budget_ns, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
+    uint32_t acc_phase = 0;
+    for (bool more = it.first_chunk(); more; more = it.next()) {
+      uint32_t got = 0;
+      if (lane == 0) got = mbar_wait_bounded(acc_full, acc_phase, args.budget_ns, abort_flag) ? 1u : 0u;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) {
+          report_timeout(args.status, kWhereEpiAccFull);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const int N = round16(it.nch);
+      const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+      const int unit_row = it.mb * kBM + q * 32 + lane;  // row of this lane inside the expert
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t r0[16];
+        tmem_ld_32x32b_x16(tmem + lane_base + (uint32_t)c0, r0);
+        if (M == Mode::GateUp) {
+          uint32_t r1[16];
+          tmem_ld_32x32b_x16(tmem + lane_base + (uint32_t)(C::kAccCol2 + c0), r1);
+          tmem_ld_wait();
+          const int i = unit_row;  // feature index in [0, f)
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = c0 + jj;
+            const float g = __uint_as_float(r0[jj]), u = __uint_as_float(r1[jj]);
+            const float h = g / (1.f + expf(-g)) * u;
+            if (col < it.nch) {
+              const size_t row = (size_t)(prow + col);
+              if (args.h16 != nullptr) {
+                args.h16[row * args.f + i] = __float2half_rn(h);
+              } else {
+                const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+                const float amax = __uint_as_float(amax_bits);
+                int s = 0;
+                if (amax > 0.f) s = max(-127, min(127, floor_log2_f32(amax) - 8));
+                const uint8_t code = (uint8_t)(f32x2_to_e4m3x2(h * exp2i(-s), 0.f) & 0xFFu);
+                args.hq[row * args.f + i] = code;
+                if (lane == 0) {
+                  const int kblk = i / 32;
+                  args.hsf[((row / 128) * (size_t)(args.f / 128) + kblk / 4) * kSfChunk + (row % 32) * 16 +
+                           ((row % 128) / 32) * 4 + (kblk % 4)] = (uint8_t)(s + 127);
+                }
+              }
+            }
+          }
+        } else {
+          tmem_ld_wait();
+          const int m = unit_row;  // output feature
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = c0 + jj;
+            if (col < it.nch) {
+              const int pair = __ldg(args.pad_pair + prow + col);
+              const int t = pair / args.k;
+              const float wv = __ldg(args.topk_w + pair);
+              red_add_f32(args.out + (size_t)t * args.d + m, wv * __uint_as_float(r0[jj]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <Mode M>
+cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                        const GemmArgs& args, cudaStream_t st) {
+  static_assert(Smem<M>::kTotal <= 227 * 1024, "shared memory");
+  const void* fn = (const void*)grouped_gemm_kernel<M>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<M>::kTotal);
+  if (e != cudaSuccess) return e;
+  const int units = args.E * (args.rows_per_expert / kBM);
+  const int grid = units < L->num_sms ? units : L->num_sms;
+  grouped_gemm_kernel<M><<<grid, 192, Smem<M>::kTotal, st>>>(a0, a1, b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st) {
+  const int blocks = (T + 7) / 8;
+  act_quant_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T, L->cfg.d_model, L->cfg.top_k,
+                                           L->s.pad_inv, L->s.xq, L->s.xsf, out);
+  return cudaGetLastError();
+}
+
+static GemmArgs base_args(const ds4moe_layer* L) {
+  GemmArgs a{};
+  a.counts = L->s.counts;
+  a.pad_offsets = L->s.pad_offsets;
+  a.pad_pair = L->s.pad_pair;
+  a.topk_w = L->s.topk_w;
+  a.E = L->cfg.n_experts;
+  a.k = L->cfg.top_k;
+  a.d = L->cfg.d_model;
+  a.f = L->cfg.d_ff;
+  a.status = L->status;
+  a.debug_fault = L->cfg.debug_fault;
+  a.budget_ns = L->cfg.debug_fault ? 1000000ull : (uint64_t)L->cfg.wait_timeout_ms * 1000000ull;
+  return a;
+}
+
+cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, cudaStream_t st) {
+  (void)T;
+  GemmArgs a = base_args(L);
+  a.sfa0 = L->w.gate_sf;
+  a.sfa1 = L->w.up_sf;
+  a.rows_per_expert = L->cfg.d_ff;
+  a.K = L->cfg.d_model;
+  a.sfb = L->s.xsf;
+  a.hq = L->s.hq;
+  a.hsf = L->s.hsf;
+  a.h16 = (L->cfg.down_format == DS4MOE_DOWN_Q2K) ? L->s.h16 : nullptr;
+  return launch_gemm<Mode::GateUp>(L, L->tm_gate, L->tm_up, L->tm_xq, a, st);
+}
+
+cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
+  (void)T;
+  GemmArgs a = base_args(L);
+  a.debug_fault = 0;
+  a.sfa0 = L->w.down_sf;
+  a.sfa1 = L->w.down_sf;
+  a.rows_per_expert = L->cfg.d_model;
+  a.K = L->cfg.d_ff;
+  a.sfb = L->s.hsf;
+  a.out = out;
+  return launch_gemm<Mode::Down>(L, L->tm_down, L->tm_down, L->tm_hq, a, st);
+}
+
+cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
+  (void)L; (void)out; (void)T; (void)st;
+  return cudaErrorNotSupported;
+}
+
+int prefill_launches() { return 5; }
+
+}  // namespace ds4moe

@@ -1,0 +1,83 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/ds4moe.h declares, and rejects bad arguments on the host before any
+device work.  No compute calls are made."""
+import ctypes
+
+import quantized_moe_expert_top_gb300 as m
+
+
+def test_library_builds_and_exports_every_header_symbol(ds4):
+    names = m.header_functions()
+    assert len(names) >= 10
+    L = ds4.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings(ds4):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = ds4.status_string(code)
+        assert s and s != "unknown status"
+    assert ds4.status_string(-99) == "unknown status"
+
+
+def test_defaults(ds4):
+    c = ds4.default_config()
+    assert (c.d_model, c.n_experts, c.d_ff, c.top_k, c.max_tokens) == (0, 0, 0, 0, 0)
+    assert c.decode_max_tokens == 64 and c.wait_timeout_ms == 2000
+    assert c.force_path == ds4.PATH_AUTO and c.debug_fault == 0
+
+
+def test_null_handles(ds4):
+    L = ds4.lib()
+    assert L.ds4moe_path_for(None, 1) == ds4.ERR_INVALID_ARG
+    assert L.ds4moe_launches_per_forward(None, 1) == ds4.ERR_INVALID_ARG
+    assert L.ds4moe_forward(None, None, None, None, 1, None) == ds4.ERR_INVALID_ARG
+    assert L.ds4moe_get_status(None) == ds4.ERR_INVALID_ARG
+    assert L.ds4moe_get_routing(None, None, None, None, None, None) == ds4.ERR_INVALID_ARG
+    L.ds4moe_destroy(None)  # NULL-safe
+
+
+def _create(ds4, **kw):
+    c = ds4.default_config()
+    c.d_model, c.n_experts, c.d_ff, c.top_k, c.max_tokens = 256, 8, 128, 2, 4
+    for k, v in kw.items():
+        setattr(c, k, v)
+    w = ds4.WeightPtrs()
+    buf = (ctypes.c_uint8 * 64)()
+    for n in ("gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales"):
+        setattr(w, n, ctypes.addressof(buf))
+    h = ctypes.c_void_p(123)
+    rc = ds4.lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h))
+    return rc, h
+
+
+def test_create_rejects_bad_shapes_on_host(ds4):
+    cases = [
+        ({"d_model": 100}, ds4.ERR_UNSUPPORTED),      # not a multiple of 128
+        ({"d_ff": 64}, ds4.ERR_UNSUPPORTED),
+        ({"n_experts": 0}, ds4.ERR_UNSUPPORTED),
+        ({"n_experts": 300}, ds4.ERR_UNSUPPORTED),
+        ({"top_k": 9}, ds4.ERR_UNSUPPORTED),
+        ({"top_k": 0}, ds4.ERR_UNSUPPORTED),
+        ({"max_tokens": 0}, ds4.ERR_INVALID_ARG),
+        ({"down_format": 7}, ds4.ERR_INVALID_ARG),
+        ({"down_format": 1, "d_ff": 384}, ds4.ERR_UNSUPPORTED),  # Q2_K needs f % 256 == 0
+        ({"force_path": 5}, ds4.ERR_INVALID_ARG),
+        ({"wait_timeout_ms": 0}, ds4.ERR_INVALID_ARG),
+        ({"decode_max_tokens": -1}, ds4.ERR_INVALID_ARG),
+    ]
+    for kw, want in cases:
+        rc, h = _create(ds4, **kw)
+        assert rc == want, (kw, rc)
+        assert h.value is None, kw  # *out cleared on failure
+
+
+def test_create_rejects_null_weights(ds4):
+    c = ds4.default_config()
+    c.d_model, c.n_experts, c.d_ff, c.top_k, c.max_tokens = 256, 8, 128, 2, 4
+    w = ds4.WeightPtrs()
+    h = ctypes.c_void_p()
+    assert ds4.lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h)) == ds4.ERR_INVALID_ARG
+    assert ds4.lib().ds4moe_layer_create(ctypes.byref(c), None, ctypes.byref(h)) == ds4.ERR_INVALID_ARG
+    assert ds4.lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), None) == ds4.ERR_INVALID_ARG
