@@ -76,13 +76,15 @@ enum { DS4MOE_DOWN_MXFP4 = 0, DS4MOE_DOWN_Q2K = 1 };
 enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2 };
 
 /* Layer shape and options.  Fill with ds4moe_config_default() first.
- *   d_model    hidden size d; multiple of 128, 128..16384.
+ *   d_model    hidden size d; multiple of 128, 128..8192.
  *   n_experts  routed experts E; 1..256.
  *   d_ff       expert intermediate size f; multiple of 128 (MXFP4 down) or
- *              of 256 (Q2_K down), 128..16384.
+ *              of 256 (Q2_K down), 128..8192.
  *   top_k      experts per token k; 1..min(8, E).
  *   max_tokens largest T a forward call may pass (scratch is sized for it).
- *   down_format      DS4MOE_DOWN_MXFP4 or DS4MOE_DOWN_Q2K.
+ *   down_format      DS4MOE_DOWN_MXFP4 or DS4MOE_DOWN_Q2K.  A Q2_K layer runs
+ *                    every call on the PREFILL path (DECODE streams MXFP4 only;
+ *                    force_path = DECODE is then UNSUPPORTED).
  *   decode_max_tokens  AUTO path choice: T <= this runs DECODE (default 64).
  *   force_path       DS4MOE_PATH_* (AUTO by default; tests force a path).
  *   debug_fault      0 in production.  1 = the first prefill GEMM drops one
@@ -168,6 +170,18 @@ int ds4moe_path_for(const ds4moe_layer *layer, int32_t T);
 /* Number of kernels one ds4moe_forward(T) enqueues (0 for T = 0), or a
  * negative error. */
 int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
+
+/* Per-kernel timing (diagnostics; off by default).  While enabled, every
+ * forward also records a CUDA event on its stream before its first kernel and
+ * after each kernel.  ds4moe_kernel_times() synchronises that stream and writes
+ * the elapsed milliseconds of each kernel of the most recent forward, in
+ * launch order (DECODE: route_topk, route_group, decode_gateup, decode_down;
+ * PREFILL: route_topk, route_group, act_quant, gemm_gateup, gemm_down), and
+ * returns how many it wrote (at most max_n), or a negative error.
+ * ds4moe_kernel_name() gives those names (NULL past the end). */
+int ds4moe_set_kernel_timing(ds4moe_layer *layer, int enable);
+int ds4moe_kernel_times(ds4moe_layer *layer, float *ms, int max_n);
+const char *ds4moe_kernel_name(int path, int i);
 
 /* Static, human-readable name of a status code. */
 const char *ds4moe_status_string(int status);

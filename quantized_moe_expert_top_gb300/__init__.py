@@ -14,5 +14,5 @@ from ._binding import (  # noqa: F401
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile libds4moe.so for sm_103a (no-op when up to date)."""
-    from .build import build as _build
+    from ._builder import build as _build
     return _build(force=force, verbose=verbose)

@@ -64,7 +64,7 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "`python quantized_moe_expert_top_gb300/build.py` (or __graft_entry__.build())")
+                               "`python quantized_moe_expert_top_gb300/_builder.py` (or __graft_entry__.build())")
         L = ctypes.CDLL(LIB_PATH)
         vp, i32 = ctypes.c_void_p, ctypes.c_int32
         L.ds4moe_config_default.restype = None
@@ -83,6 +83,12 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_path_for.argtypes = [vp, i32]
         L.ds4moe_launches_per_forward.restype = ctypes.c_int
         L.ds4moe_launches_per_forward.argtypes = [vp, i32]
+        L.ds4moe_set_kernel_timing.restype = ctypes.c_int
+        L.ds4moe_set_kernel_timing.argtypes = [vp, ctypes.c_int]
+        L.ds4moe_kernel_times.restype = ctypes.c_int
+        L.ds4moe_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
+        L.ds4moe_kernel_name.restype = ctypes.c_char_p
+        L.ds4moe_kernel_name.argtypes = [ctypes.c_int, ctypes.c_int]
         L.ds4moe_status_string.restype = ctypes.c_char_p
         L.ds4moe_status_string.argtypes = [ctypes.c_int]
         L.ds4moe_destroy.restype = None
@@ -206,6 +212,20 @@ class Layer:
 
     def launches_per_forward(self, T: int) -> int:
         return lib().ds4moe_launches_per_forward(self._h, T)
+
+    def set_kernel_timing(self, enable: bool):
+        rc = lib().ds4moe_set_kernel_timing(self._h, 1 if enable else 0)
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_set_kernel_timing")
+
+    def kernel_times(self) -> dict:
+        """{kernel name: ms} of the most recent forward (timing must be on)."""
+        buf = (ctypes.c_float * 8)()
+        n = lib().ds4moe_kernel_times(self._h, buf, 8)
+        if n < 0:
+            raise Ds4moeError(n, "ds4moe_kernel_times")
+        path = self.path_for(self._last_T)
+        return {lib().ds4moe_kernel_name(path, i).decode(): float(buf[i]) for i in range(n)}
 
     def close(self):
         if self._h is not None:

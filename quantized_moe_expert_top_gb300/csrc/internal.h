@@ -72,6 +72,9 @@ struct ds4moe_layer {
   CUtensorMap tm_xq;    // 8-bit activations, box 128 x 32
   CUtensorMap tm_hq;
   CUtensorMap tm_h16;   // fp16 h, box 64 x 32
+  cudaEvent_t ev[8];   // kernel timing events (created when timing is enabled)
+  bool timing;
+  int last_nk;         // kernels in the most recent forward
   int last_T;
   cudaStream_t last_stream;
   bool has_forward;

@@ -339,19 +339,29 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   if (cudaGetDevice(&cur) != cudaSuccess || cur != L->device) return DS4MOE_ERR_INVALID_ARG;
 
   L->last_stream = st;
-  cudaError_t e = launch_route_topk(logits, T, L->cfg.n_experts, L->cfg.top_k, L->s.topk_idx, L->s.topk_w, st);
-  if (e == cudaSuccess) e = launch_route_group(L, T, st);
+  int nk = 0;
+  auto mark = [&](cudaError_t e) {
+    if (e == cudaSuccess && L->timing) e = cudaEventRecord(L->ev[nk], st);
+    ++nk;
+    return e;
+  };
+  cudaError_t e = L->timing ? cudaEventRecord(L->ev[0], st) : cudaSuccess;
+  nk = 1;
+  if (e == cudaSuccess)
+    e = mark(launch_route_topk(logits, T, L->cfg.n_experts, L->cfg.top_k, L->s.topk_idx, L->s.topk_w, st));
+  if (e == cudaSuccess) e = mark(launch_route_group(L, T, st));
   if (path == DS4MOE_PATH_DECODE) {
-    if (e == cudaSuccess) e = launch_decode_gateup(L, x, out, T, st);
-    if (e == cudaSuccess) e = launch_decode_down(L, out, T, st);
+    if (e == cudaSuccess) e = mark(launch_decode_gateup(L, x, out, T, st));
+    if (e == cudaSuccess) e = mark(launch_decode_down(L, out, T, st));
   } else {
-    if (e == cudaSuccess) e = launch_act_quant(L, x, out, T, st);
-    if (e == cudaSuccess) e = launch_gemm_gateup(L, T, st);
+    if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, st));
+    if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, st));
     if (e == cudaSuccess) {
-      if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = launch_gemm_down_q2k(L, out, T, st);
-      else e = launch_gemm_down(L, out, T, st);
+      if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = mark(launch_gemm_down_q2k(L, out, T, st));
+      else e = mark(launch_gemm_down(L, out, T, st));
     }
   }
+  L->last_nk = nk - 1;
   if (e != cudaSuccess) {
     cudaGetLastError();
     return DS4MOE_ERR_CUDA;
@@ -421,8 +431,47 @@ int ds4moe_get_status(ds4moe_layer* L) {
   return DS4MOE_OK;
 }
 
+int ds4moe_set_kernel_timing(ds4moe_layer* L, int enable) {
+  if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (enable && !L->ev[0]) {
+    for (int i = 0; i < 8; ++i)
+      if (cudaEventCreate(&L->ev[i]) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ERR_CUDA;
+      }
+  }
+  L->timing = enable != 0;
+  return DS4MOE_OK;
+}
+
+int ds4moe_kernel_times(ds4moe_layer* L, float* ms, int max_n) {
+  if (!L || !ms || max_n < 0) return DS4MOE_ERR_INVALID_ARG;
+  if (!L->timing || !L->has_forward) return DS4MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(L->last_stream) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  const int n = L->last_nk < max_n ? L->last_nk : max_n;
+  for (int i = 0; i < n; ++i)
+    if (cudaEventElapsedTime(&ms[i], L->ev[i], L->ev[i + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return DS4MOE_ERR_CUDA;
+    }
+  return n;
+}
+
+const char* ds4moe_kernel_name(int path, int i) {
+  static const char* dec[] = {"route_topk", "route_group", "decode_gateup", "decode_down"};
+  static const char* pre[] = {"route_topk", "route_group", "act_quant", "gemm_gateup", "gemm_down"};
+  if (path == DS4MOE_PATH_DECODE && i >= 0 && i < 4) return dec[i];
+  if (path == DS4MOE_PATH_PREFILL && i >= 0 && i < 5) return pre[i];
+  return nullptr;
+}
+
 void ds4moe_destroy(ds4moe_layer* L) {
   if (!L) return;
+  for (int i = 0; i < 8; ++i)
+    if (L->ev[i]) cudaEventDestroy(L->ev[i]);
   free_all(L);
   delete L;
 }

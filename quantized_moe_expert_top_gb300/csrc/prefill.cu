@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
         const int nb = (N + 31) / 32, nsf = (N + 127) / 128;
         const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
         const int arow = it.e * args.rows_per_expert + it.mb * kBM;
-        const uint32_t bytes = (uint32_t)(C::kNumA * S::kA + nb * 32 * kBK + (C::kNumA + nsf) * kSfChunk);
+        // A 4-bit unpacking load counts its packed global bytes (half the
+        // 16 KB it writes to shared memory).
+        const uint32_t bytes = (uint32_t)(C::kNumA * S::kA / 2 + nb * 32 * kBK + (C::kNumA + nsf) * kSfChunk);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
