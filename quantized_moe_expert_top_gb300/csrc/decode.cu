@@ -1,17 +1,25 @@
 // Few-token (decode) path of the routed-MoE layer: memory-bound GEMVs over
 // the routed experts' MXFP4 weights.
 //
-// Each warp streams whole weight rows with 128-bit non-coherent loads (one
-// 16-byte chunk = one 32-element MXFP4 block per lane and step), converts the
-// E2M1 codes to f16 in registers with the hardware e2m1x2 conversion, and
-// accumulates f16 x f16 products in fp32 (mixed-precision FMA; the products
-// are exact).  The per-block E8M0 scale multiplies each block's partial sum.
-// Lanes are then reduced with shuffles.
+// Each CTA owns a contiguous run of weight rows of the touched experts and
+// streams them through a shared-memory ring: one thread issues bulk copies
+// (cp.async.bulk, whole interleaved rows: codes and their E8M0 scales) several
+// stages ahead, so many kilobytes per SM are always in flight; eight consumer
+// warps each take one row (gate/up: one gate+up row pair) per stage.  A
+// consumer lane reads 16-byte chunks (one 32-element MXFP4 block each),
+// converts the E2M1 codes to f16 in registers with the hardware e2m1x2
+// conversion, multiplies by the activations, scales each block's partial sum
+// by its E8M0 scale, and the warp reduces its lanes with shuffles.
 //
-// Activations enter as f16 with a power-of-two prescale per row (so any bf16 /
-// fp32 magnitude maps into f16's range without overflow; the scale is undone
-// exactly on the fp32 result).  x is exact in f16 after prescaling (bf16 has 8
-// significant bits); h loses only its bits beyond f16's 11.
+//   gate/up : x arrives as f16 with a per-token power-of-two prescale (made by
+//             the top-k kernel); f16 x f16 products are exact in the fp32
+//             mixed-precision FMA, so x enters exactly.  h = SwiGLU(g, u) is
+//             stored in fp32.
+//   down    : h is used in fp32 (weights converted f16 -> f32); the weighted
+//             combine red-adds w[t,j] * y into out[t], which the gate/up kernel
+//             zeroed.
+// Activations are read through L1 (every warp of an SM reads the same few
+// token rows).  Every mbarrier wait is bounded (see the prefill GEMM).
 //
 // Pages: "DwarfStar実地分析" §GGUFの対応範囲は意図的に狭い (MXFP4 routed experts);
 // "284B MoEを128GBノートPCに詰め込む" §プリフィル790 t/sが暴く真のボトルネック
@@ -22,11 +30,12 @@
 namespace ds4moe {
 namespace {
 
-constexpr int kNT = 8;           // tokens per pass (activations staged in shared memory)
-constexpr int kThreads = 256;    // 8 warps
-constexpr int kGateUpRowsPerItem = 8;   // row pairs per work item (one per warp)
-constexpr int kDownRowsPerWarp = 4;
-constexpr int kDownRowsPerItem = kDownRowsPerWarp * (kThreads / 32);
+constexpr int kNT = 8;            // tokens per pass over a row
+constexpr int kConsumers = 8;     // consumer warps
+constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr int kRingBytes = 200 * 1024;
+constexpr int kMaxStages = 8;
+constexpr int kDnRowsPerWarp = 4;
 
 __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
   if (b == 0u) return __int_as_float(0x00400000);  // 2^-127
@@ -34,288 +43,322 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
   return __int_as_float((int)(b << 23));
 }
 
-// Shared-memory layout of one staged activation row of K elements as f16:
-// 16-byte piece q (elements 8q'..8q'+7 of 32-element block c, q' = 0..3) sits at
-// piece index q'*nblk + c, so lane l reading block c = l + 32i hits
-// consecutive 16-byte words (no bank conflicts).
-__device__ __forceinline__ int piece_index(int c, int q, int nblk) { return q * nblk + c; }
+__device__ __forceinline__ uint4 ldg_l1(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
 
-// Stage `nt` activation rows into shared memory as prescaled f16.
-// src(row r) is bf16 (is_bf16) or fp32; element offset row_off(tt).
-template <bool kBf16>
-__device__ void stage_rows(const void* __restrict__ src, const int32_t* __restrict__ rows, int nt, int K,
-                           uint4* __restrict__ xs, float* __restrict__ sig) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nblk = K / 32;
-  for (int tt = wid; tt < nt; tt += kThreads / 32) {
-    const size_t r = (size_t)rows[tt];
-    // pass 1: amax over the row
-    float amax = 0.f;
-    if (kBf16) {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + r * K);
-      for (int i = lane; i < K / 8; i += 32) {
-        const uint4 v = __ldg(p + i);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(wv[q] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(wv[q] & 0xFFFF0000u)));
-        }
-      }
-    } else {
-      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + r * K);
-      for (int i = lane; i < K / 4; i += 32) {
-        const float4 v = p[i];
-        amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-      }
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// Index of h[pair][i] in the piece-transposed fp32 layout the down kernel
+// reads: 16-byte piece j (4 floats) of 32-element block c at (j * f/32 + c).
+__device__ __forceinline__ size_t h_index(int pair, int i, int f) {
+  const int c = i >> 5, j = (i >> 2) & 7;
+  return (size_t)pair * f + ((size_t)j * (f >> 5) + c) * 4 + (i & 3);
+}
+
+struct Ring {
+  uint8_t* buf;
+  uint64_t* full;
+  uint64_t* empty;
+  int stages, stage_bytes;
+};
+
+// Producer: stage s of this CTA holds rows [r0 + s*rps, r0 + (s+1)*rps) of the
+// global row list (clipped to r1); row r lives at base + grow(r) * pitch where
+// consecutive rows of one expert are consecutive in memory.
+template <typename RowAddr>
+__device__ void produce(const Ring& R, int r0, int r1, int rps, int pitch, RowAddr row_addr, uint64_t budget,
+                        DeviceStatus* status, volatile int* abort_flag) {
+  const int nst = (r1 - r0 + rps - 1) / rps;
+  uint32_t issued = 0, parity = 0;
+  for (int s = 0; s < nst; ++s) {
+    const int slot = s % R.stages;
+    const uint32_t ph = (uint32_t)(s / R.stages) & 1u;
+    if (!mbar_wait_bounded(&R.empty[slot], ph ^ 1u, budget, abort_flag)) {
+      report_timeout(status, kWhereProducerEmpty);
+      *abort_flag = 1;
+      break;
     }
-    amax = warp_max(amax);
-    const int s = f16_prescale_exp(amax);
-    const float inv = exp2i(-s);
-    if (lane == 0) sig[tt] = exp2i(s);
-    // pass 2: convert, 8 elements (one 16-byte piece of f16) per step
-    uint4* dst = xs + (size_t)tt * (K / 8);
-    for (int i = lane; i < K / 8; i += 32) {
-      float f[8];
-      if (kBf16) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + r * K) + i);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          f[2 * q] = __uint_as_float(wv[q] << 16);
-          f[2 * q + 1] = __uint_as_float(wv[q] & 0xFFFF0000u);
-        }
-      } else {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + r * K);
-        const float4 a = p[2 * i], b = p[2 * i + 1];
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-      }
-      uint32_t h[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const __half2 hv = __floats2half2_rn(f[2 * q] * inv, f[2 * q + 1] * inv);
-        h[q] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      const int c = i >> 2, q = i & 3;  // block c, piece q
-      dst[piece_index(c, q, nblk)] = make_uint4(h[0], h[1], h[2], h[3]);
+    const int a = r0 + s * rps, b = min(a + rps, r1);
+    mbar_arrive_expect_tx(&R.full[slot], (uint32_t)((b - a) * pitch));
+    uint8_t* dst = R.buf + slot * R.stage_bytes;
+    int seg = a;
+    while (seg < b) {  // contiguous segments (an expert boundary breaks a stage)
+      const uint8_t* src = row_addr(seg);
+      int end = seg + 1;
+      while (end < b && row_addr(end) == src + (size_t)(end - seg) * pitch) ++end;
+      bulk_load(dst + (size_t)(seg - a) * pitch, src, (uint32_t)((end - seg) * pitch), &R.full[slot]);
+      seg = end;
     }
+    issued |= 1u << slot;
+    parity = (parity & ~(1u << slot)) | (ph << slot);
+  }
+  if (*abort_flag) {
+    for (int slot = 0; slot < R.stages; ++slot)
+      if ((issued >> slot) & 1u) {
+        volatile int never = 0;
+        mbar_wait_bounded(&R.full[slot], (parity >> slot) & 1u, budget, &never);
+      }
   }
 }
 
-// Dot products of R weight rows (MXFP4, K elements each) with nt staged
-// activation rows.  acc[r][tt] receives lane-partial sums (reduce afterwards).
-template <int R, int CPL>
-__device__ __forceinline__ void rows_dot(const uint8_t* const (&codes)[R], const uint8_t* const (&scales)[R],
-                                         int nblk, const uint4* __restrict__ xs, int nt,
-                                         float (&acc)[R][kNT]) {
-  const int lane = threadIdx.x & 31;
-  const int xstride = nblk * 4;  // uint4 pieces per staged row
-  for (int c0 = 0; c0 < nblk; c0 += 32 * CPL) {
-    uint4 cw[R][CPL];
-    uint32_t sb[R][CPL];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int q = 0; q < CPL; ++q) {
-        const int c = c0 + lane + 32 * q;
-        if (c < nblk) {
-          cw[r][q] = ldg_nc_v4(codes[r] + (size_t)c * 16);
-          sb[r][q] = __ldg(scales[r] + c);
-        } else {
-          cw[r][q] = make_uint4(0, 0, 0, 0);
-          sb[r][q] = 127u;
-        }
-      }
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-      const int c = c0 + lane + 32 * q;
-      if (c >= nblk) break;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        uint32_t wh[16];
-        const uint32_t words[4] = {cw[r][q].x, cw[r][q].y, cw[r][q].z, cw[r][q].w};
-#pragma unroll
-        for (int b = 0; b < 16; ++b) wh[b] = e2m1x2_to_f16x2((words[b >> 2] >> (8 * (b & 3))) & 0xFFu);
-        const float sc = e8m0_to_f32(sb[r][q]);
-#pragma unroll
-        for (int tt = 0; tt < kNT; ++tt) {
-          if (tt < nt) {
-            float p = 0.f;
-#pragma unroll
-            for (int pq = 0; pq < 4; ++pq) {
-              const uint4 xv = xs[(size_t)tt * xstride + piece_index(c, pq, nblk)];
-              p = dot2_f16_f32(wh[4 * pq + 0], xv.x, p);
-              p = dot2_f16_f32(wh[4 * pq + 1], xv.y, p);
-              p = dot2_f16_f32(wh[4 * pq + 2], xv.z, p);
-              p = dot2_f16_f32(wh[4 * pq + 3], xv.w, p);
-            }
-            acc[r][tt] = fmaf(p, sc, acc[r][tt]);
-          }
-        }
-      }
+// Consumer side of one stage: wait (lane 0, bounded) and broadcast the outcome.
+__device__ __forceinline__ bool consume_wait(const Ring& R, int s, uint64_t budget, DeviceStatus* status,
+                                             volatile int* abort_flag) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) {
+    ok = mbar_wait_bounded(&R.full[s % R.stages], (uint32_t)(s / R.stages) & 1u, budget, abort_flag) ? 1u : 0u;
+    if (!ok) {
+      report_timeout(status, kWhereMmaFull);
+      *abort_flag = 1;
     }
   }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Gate/up + SwiGLU.  Work item = (touched expert, block of 8 row pairs); one
-// warp per row pair (gate row i and up row i of the expert).  Also zeroes `out`
-// for the down kernel's weighted accumulation.
-__global__ void __launch_bounds__(kThreads) decode_gateup_kernel(
-    const uint8_t* __restrict__ gate_codes, const uint8_t* __restrict__ gate_scales,
-    const uint8_t* __restrict__ up_codes, const uint8_t* __restrict__ up_scales, const void* __restrict__ x,
+__device__ __forceinline__ void consume_release(const Ring& R, int s) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[s % R.stages]);
+}
+
+__device__ __forceinline__ void cta_range(int total, int& r0, int& r1) {
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  r0 = min((int)blockIdx.x * per, total);
+  r1 = min(r0 + per, total);
+}
+
+__device__ Ring setup_ring(uint8_t* smem_raw, int stage_bytes) {
+  Ring R;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  R.stages = min(kMaxStages, kRingBytes / stage_bytes);
+  R.stage_bytes = stage_bytes;
+  R.full = reinterpret_cast<uint64_t*>(base);
+  R.empty = R.full + kMaxStages;
+  R.buf = base + 256;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R.stages; ++i) {
+      mbar_init(&R.full[i], 1);
+      mbar_init(&R.empty[i], kConsumers);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  return R;
+}
+
+// ------------------------------------------------------------------ gate/up
+// Rows = every (gate row i, up row i) pair of every touched expert (one
+// interleaved gu row each); stage = kConsumers rows, one per consumer warp.
+__global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
+    const uint8_t* __restrict__ gu, int pitch, const uint4* __restrict__ xh, const float* __restrict__ xsig,
     float* __restrict__ out, int T, int d, int f, const int32_t* __restrict__ touched,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_tok, float* __restrict__ h_dec, int E) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint4* xs = reinterpret_cast<uint4*>(smem);
-  __shared__ float sig[kNT];
-  __shared__ int32_t rows[kNT];
-
-  {  // zero out[T][d]
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_tok, float* __restrict__ h_dec, int E,
+    DeviceStatus* status, uint64_t budget) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  if (threadIdx.x == 0) abort_s = 0;
+  {  // zero out[T][d] for the down kernel's accumulation
     float4* o4 = reinterpret_cast<float4*>(out);
     const size_t n4 = (size_t)T * d / 4;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
       o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int n_touched = touched[E];
-  const int nblk_items = f / kGateUpRowsPerItem;
-  const int nitems = n_touched * nblk_items;
-  const int nblk = d / 32;
-  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-    const int e = touched[item / nblk_items];
-    const int i = (item % nblk_items) * kGateUpRowsPerItem + wid;
-    const int p0 = offsets[e], ne = offsets[e + 1] - p0;
-    const size_t grow = (size_t)e * f + i;
-    const uint8_t* const codes[2] = {gate_codes + grow * (d / 2), up_codes + grow * (d / 2)};
-    const uint8_t* const scales[2] = {gate_scales + grow * (d / 32), up_scales + grow * (d / 32)};
-    for (int tg = 0; tg < ne; tg += kNT) {
-      const int nt = min(kNT, ne - tg);
-      __syncthreads();  // previous users of xs / rows are done
-      if (threadIdx.x < nt) rows[threadIdx.x] = perm_tok[p0 + tg + threadIdx.x];
-      __syncthreads();
-      stage_rows<true>(x, rows, nt, d, xs, sig);
-      __syncthreads();
-      float acc[2][kNT];
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int tt = 0; tt < kNT; ++tt) acc[r][tt] = 0.f;
-      rows_dot<2, 4>(codes, scales, nblk, xs, nt, acc);
-#pragma unroll
-      for (int tt = 0; tt < kNT; ++tt) {
-        if (tt < nt) {
-          const float g = warp_sum(acc[0][tt]) * sig[tt];
-          const float u = warp_sum(acc[1][tt]) * sig[tt];
-          if (lane == tt) h_dec[(size_t)(p0 + tg + tt) * f + i] = g / (1.f + expf(-g)) * u;
-        }
-      }
-    }
+  const Ring R = setup_ring(smem_raw, kConsumers * pitch);
+  int r0, r1;
+  cta_range(touched[E] * f, r0, r1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    if (lane == 0)
+      produce(R, r0, r1, kConsumers, pitch,
+              [&](int r) { return gu + ((size_t)__ldg(touched + r / f) * f + r % f) * pitch; }, budget, status,
+              abort_flag);
+    return;
   }
-}
-
-// Down projection + weighted combine.  Work item = (touched expert, block of
-// 32 output rows); each warp handles 4 rows at once and red-adds
-// w[t,j] * y into out[t] (zeroed by the gate/up kernel).
-__global__ void __launch_bounds__(kThreads) decode_down_kernel(
-    const uint8_t* __restrict__ down_codes, const uint8_t* __restrict__ down_scales, float* __restrict__ out,
-    int d, int f, int k, const int32_t* __restrict__ touched, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ perm_tok, const int32_t* __restrict__ perm_slot, const float* __restrict__ topk_w,
-    const float* __restrict__ h_dec, int E) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint4* hs = reinterpret_cast<uint4*>(smem);
-  __shared__ float sig[kNT];
-  __shared__ int32_t rows[kNT];
-  __shared__ float wt[kNT];
-  __shared__ int32_t tok[kNT];
-
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int n_touched = touched[E];
-  const int nblk_items = d / kDownRowsPerItem;
-  const int nitems = n_touched * nblk_items;
-  const int nblk = f / 32;
-  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-    const int e = touched[item / nblk_items];
-    const int m0 = (item % nblk_items) * kDownRowsPerItem + wid * kDownRowsPerWarp;
-    const int p0 = offsets[e], ne = offsets[e + 1] - p0;
-    const uint8_t* codes[kDownRowsPerWarp];
-    const uint8_t* scales[kDownRowsPerWarp];
+  const int cw = warp - 1;
+  const int nblk = d / 32;
+  const int nst = (r1 - r0 + kConsumers - 1) / kConsumers;
+  for (int s = 0; s < nst; ++s) {
+    if (!consume_wait(R, s, budget, status, abort_flag)) return;
+    const int rp = r0 + s * kConsumers + cw;
+    if (rp < r1) {
+      const uint8_t* row = R.buf + (s % R.stages) * R.stage_bytes + cw * pitch;
+      const int e = __ldg(touched + rp / f), i = rp % f;
+      const int p0 = __ldg(offsets + e), ne = __ldg(offsets + e + 1) - p0;
+      for (int tg = 0; tg < ne; tg += kNT) {
+        const int nt = min(kNT, ne - tg);
+        const int my_tok = lane < nt ? __ldg(perm_tok + p0 + tg + lane) : 0;
+        int toks[kNT];
+        float ag[kNT], au[kNT];
 #pragma unroll
-    for (int r = 0; r < kDownRowsPerWarp; ++r) {
-      const size_t grow = (size_t)e * d + m0 + r;
-      codes[r] = down_codes + grow * (f / 2);
-      scales[r] = down_scales + grow * (f / 32);
-    }
-    for (int tg = 0; tg < ne; tg += kNT) {
-      const int nt = min(kNT, ne - tg);
-      __syncthreads();
-      if (threadIdx.x < nt) {
-        const int p = p0 + tg + threadIdx.x;
-        const int t = perm_tok[p];
-        rows[threadIdx.x] = p;
-        tok[threadIdx.x] = t;
-        wt[threadIdx.x] = topk_w[(size_t)t * k + perm_slot[p]];
-      }
-      __syncthreads();
-      stage_rows<false>(h_dec, rows, nt, f, hs, sig);
-      __syncthreads();
-      float acc[kDownRowsPerWarp][kNT];
+        for (int tt = 0; tt < kNT; ++tt) {
+          toks[tt] = __shfl_sync(0xffffffffu, my_tok, tt);  // warp converged here
+          ag[tt] = au[tt] = 0.f;
+        }
+        for (int c = lane; c < nblk; c += 32) {
+          const uint4 gq = lds128(row + 16 * c), uq = lds128(row + d / 2 + 16 * c);
+          const float sg = e8m0_to_f32(row[d + c]), su = e8m0_to_f32(row[d + d / 32 + c]);
+          uint32_t wg[16], wu[16];
+          const uint32_t g4[4] = {gq.x, gq.y, gq.z, gq.w}, u4[4] = {uq.x, uq.y, uq.z, uq.w};
 #pragma unroll
-      for (int r = 0; r < kDownRowsPerWarp; ++r)
+          for (int b = 0; b < 16; ++b) {
+            wg[b] = e2m1x2_to_f16x2((g4[b >> 2] >> (8 * (b & 3))) & 0xFFu);
+            wu[b] = e2m1x2_to_f16x2((u4[b >> 2] >> (8 * (b & 3))) & 0xFFu);
+          }
 #pragma unroll
-        for (int tt = 0; tt < kNT; ++tt) acc[r][tt] = 0.f;
-      rows_dot<kDownRowsPerWarp, 2>(codes, scales, nblk, hs, nt, acc);
+          for (int tt = 0; tt < kNT; ++tt) {
+            if (tt < nt) {
+              const uint4* xr = xh + (size_t)toks[tt] * (d / 8);
+              float pg = 0.f, pu = 0.f;
 #pragma unroll
-      for (int r = 0; r < kDownRowsPerWarp; ++r)
+              for (int pq = 0; pq < 4; ++pq) {
+                const uint4 xv = ldg_l1(xr + pq * nblk + c);
+                pg = dot2_f16_f32(wg[4 * pq + 0], xv.x, pg);
+                pg = dot2_f16_f32(wg[4 * pq + 1], xv.y, pg);
+                pg = dot2_f16_f32(wg[4 * pq + 2], xv.z, pg);
+                pg = dot2_f16_f32(wg[4 * pq + 3], xv.w, pg);
+                pu = dot2_f16_f32(wu[4 * pq + 0], xv.x, pu);
+                pu = dot2_f16_f32(wu[4 * pq + 1], xv.y, pu);
+                pu = dot2_f16_f32(wu[4 * pq + 2], xv.z, pu);
+                pu = dot2_f16_f32(wu[4 * pq + 3], xv.w, pu);
+              }
+              ag[tt] = fmaf(pg, sg, ag[tt]);
+              au[tt] = fmaf(pu, su, au[tt]);
+            }
+          }
+        }
 #pragma unroll
         for (int tt = 0; tt < kNT; ++tt) {
           if (tt < nt) {
-            const float y = warp_sum(acc[r][tt]) * sig[tt];
-            if (lane == tt) red_add_f32(out + (size_t)tok[tt] * d + m0 + r, wt[tt] * y);
+            const float sig = __ldg(xsig + toks[tt]);
+            const float g = warp_sum(ag[tt]) * sig;
+            const float u = warp_sum(au[tt]) * sig;
+            if (lane == tt) h_dec[h_index(p0 + tg + tt, i, f)] = __fdividef(g, 1.f + __expf(-g)) * u;
           }
         }
+      }
     }
+    consume_release(R, s);
   }
+}
+
+// ------------------------------------------------------------------ down
+// Rows = every output row of every touched expert (one dn row each); stage =
+// kConsumers * 4 rows, four per consumer warp.
+__global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(
+    const uint8_t* __restrict__ dn, int pitch, float* __restrict__ out, int d, int f, int k,
+    const int32_t* __restrict__ touched, const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_tok,
+    const int32_t* __restrict__ perm_slot, const float* __restrict__ topk_w, const float* __restrict__ h_dec, int E,
+    DeviceStatus* status, uint64_t budget) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  if (threadIdx.x == 0) abort_s = 0;
+  constexpr int rps = kConsumers * kDnRowsPerWarp;
+  const Ring R = setup_ring(smem_raw, rps * pitch);
+  int r0, r1;
+  cta_range(touched[E] * d, r0, r1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    if (lane == 0)
+      produce(R, r0, r1, rps, pitch, [&](int r) { return dn + ((size_t)__ldg(touched + r / d) * d + r % d) * pitch; },
+              budget, status, abort_flag);
+    return;
+  }
+  const int cw = warp - 1;
+  const int nblk = f / 32;
+  const int nst = (r1 - r0 + rps - 1) / rps;
+  for (int s = 0; s < nst; ++s) {
+    if (!consume_wait(R, s, budget, status, abort_flag)) return;
+    const uint8_t* stage = R.buf + (s % R.stages) * R.stage_bytes;
+#pragma unroll 1
+    for (int rr = 0; rr < kDnRowsPerWarp; ++rr) {
+      const int r = r0 + s * rps + cw * kDnRowsPerWarp + rr;
+      if (r >= r1) break;
+      const uint8_t* row = stage + (cw * kDnRowsPerWarp + rr) * pitch;
+      const int e = __ldg(touched + r / d), m = r % d;
+      const int p0 = __ldg(offsets + e), ne = __ldg(offsets + e + 1) - p0;
+      for (int tg = 0; tg < ne; tg += kNT) {
+        const int nt = min(kNT, ne - tg);
+        float acc[kNT];
+#pragma unroll
+        for (int tt = 0; tt < kNT; ++tt) acc[tt] = 0.f;
+        for (int c = lane; c < nblk; c += 32) {
+          const uint4 cq = lds128(row + 16 * c);
+          const float sc = e8m0_to_f32(row[f / 2 + c]);
+          float wf[32];
+          const uint32_t c4[4] = {cq.x, cq.y, cq.z, cq.w};
+#pragma unroll
+          for (int b = 0; b < 16; ++b) {
+            const uint32_t h2 = e2m1x2_to_f16x2((c4[b >> 2] >> (8 * (b & 3))) & 0xFFu);
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+            wf[2 * b] = v.x;
+            wf[2 * b + 1] = v.y;
+          }
+#pragma unroll
+          for (int tt = 0; tt < kNT; ++tt) {
+            if (tt < nt) {
+              const float* hp = h_dec + (size_t)(p0 + tg + tt) * f;
+              float p = 0.f;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint4 hv4 = ldg_l1(hp + ((size_t)j * nblk + c) * 4);
+                p = fmaf(wf[4 * j + 0], __uint_as_float(hv4.x), p);
+                p = fmaf(wf[4 * j + 1], __uint_as_float(hv4.y), p);
+                p = fmaf(wf[4 * j + 2], __uint_as_float(hv4.z), p);
+                p = fmaf(wf[4 * j + 3], __uint_as_float(hv4.w), p);
+              }
+              acc[tt] = fmaf(p, sc, acc[tt]);
+            }
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < kNT; ++tt) {
+          if (tt < nt) {
+            const float y = warp_sum(acc[tt]);
+            if (lane == 0) {
+              const int p = p0 + tg + tt;
+              const int t = __ldg(perm_tok + p);
+              red_add_f32(out + (size_t)t * d + m, __ldg(topk_w + (size_t)t * k + __ldg(perm_slot + p)) * y);
+            }
+          }
+        }
+      }
+    }
+    consume_release(R, s);
+  }
+}
+
+size_t ring_smem(int stage_bytes) {
+  const int stages = kRingBytes / stage_bytes < kMaxStages ? kRingBytes / stage_bytes : kMaxStages;
+  return 128 + 256 + (size_t)stages * stage_bytes;
 }
 
 }  // namespace
 
-static int grid_for(const ds4moe_layer* L, const void* kernel, size_t smem) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  return L->num_sms * per_sm;
-}
-
 cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st) {
+  (void)x;
   const int d = L->cfg.d_model, f = L->cfg.d_ff, E = L->cfg.n_experts;
-  const size_t smem = (size_t)kNT * d * 2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_set = true;
-  }
-  const int grid = grid_for(L, (const void*)decode_gateup_kernel, smem);
-  decode_gateup_kernel<<<grid, kThreads, smem, st>>>(L->w.gate_codes, L->w.gate_scales, L->w.up_codes,
-                                                     L->w.up_scales, x, out, T, d, f, L->s.touched, L->s.offsets,
-                                                     L->s.perm_tok, L->s.h_dec, E);
+  const size_t smem = ring_smem(kConsumers * L->w.pitch_gu);
+  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_gateup_kernel<<<L->num_sms, kThreads, smem, st>>>(
+      L->w.gu, L->w.pitch_gu, reinterpret_cast<const uint4*>(L->s.xh), L->s.xsig, out, T, d, f, L->s.touched,
+      L->s.offsets, L->s.perm_tok, L->s.h_dec, E, L->status, (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
   (void)T;
   const int d = L->cfg.d_model, f = L->cfg.d_ff, E = L->cfg.n_experts, k = L->cfg.top_k;
-  const size_t smem = (size_t)kNT * f * 2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_set = true;
-  }
-  const int grid = grid_for(L, (const void*)decode_down_kernel, smem);
-  decode_down_kernel<<<grid, kThreads, smem, st>>>(L->w.down_codes, L->w.down_scales, out, d, f, k, L->s.touched,
-                                                   L->s.offsets, L->s.perm_tok, L->s.perm_slot, L->s.topk_w,
-                                                   L->s.h_dec, E);
+  const size_t smem = ring_smem(kConsumers * kDnRowsPerWarp * L->w.pitch_dn);
+  cudaError_t e = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_down_kernel<<<L->num_sms, kThreads, smem, st>>>(
+      L->w.dn, L->w.pitch_dn, out, d, f, k, L->s.touched, L->s.offsets, L->s.perm_tok, L->s.perm_slot, L->s.topk_w,
+      L->s.h_dec, E, L->status, (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
   return cudaGetLastError();
 }
 

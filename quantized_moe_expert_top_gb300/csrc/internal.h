@@ -19,6 +19,7 @@ constexpr int kPadRows = 128;     // each expert's token rows start on a 128-row
 constexpr int kSfChunk = 512;     // bytes of one scale-factor chunk (128 rows x 4 blocks)
 constexpr int kGateUpNMax = 224;  // token columns per gate/up tile (two accumulators in TMEM)
 constexpr int kDownNMax = 256;    // token columns per down tile
+constexpr int kQ2kChunk = 3072;   // bytes of one Q2_K tile-major chunk
 
 // Routing tables and scratch for one forward call (all device memory).
 struct Scratch {
@@ -33,7 +34,9 @@ struct Scratch {
   int32_t* pad_inv;      // [Tmax*k]  padded row of pair (t, j)
   int32_t* pad_pair;     // [pad_rows_max] pair index t*k+j of a padded row (-1: padding)
   int32_t* touched;      // [E+1] experts with at least one token, then their count at [E]
-  float* h_dec;          // [Tdec*k][f] decode-path SwiGLU output (fp32)
+  __half* xh;            // [Tdec][d] decode-path x as prescaled f16 (piece-transposed rows)
+  float* xsig;           // [Tdec] the prescale 2^s of each row of xh
+  float* h_dec;          // [Tdec*k][f] decode-path SwiGLU output (fp32, piece-transposed rows)
   uint8_t* xq;           // [pad_rows_max][d]   MXFP8 codes of x, padded expert order
   uint8_t* xsf;          // [pad_rows_max/128][d/128][512] E8M0 scales (tcgen05 chunk layout)
   uint8_t* hq;           // [pad_rows_max][f]   MXFP8 codes of h (MXFP4 down)
@@ -46,14 +49,21 @@ struct Scratch {
 };
 
 // Weights as the kernels read them (library-owned device copies).
+//   gu: one row per (expert, i): gate codes (d/2 B) | up codes (d/2 B) |
+//       gate scales (d/32 B) | up scales (d/32 B) | padding to pitch_gu
+//       (a multiple of 32 B).  The decode path streams whole rows; the
+//       prefill TMA maps view the gate and up code columns with this pitch.
+//   dn: one row per (expert, m): codes (f/2 B) | scales (f/32 B) | padding.
 struct Weights {
-  uint8_t *gate_codes, *up_codes;  // [E][f][d/2]  canonical MXFP4 codes
-  uint8_t *gate_scales, *up_scales;  // [E][f][d/32] canonical E8M0 (decode path)
+  uint8_t* gu;                       // [E][f][pitch_gu]
+  uint8_t* dn;                       // [E][d][pitch_dn] (MXFP4 down)
+  int pitch_gu, pitch_dn;
   uint8_t *gate_sf, *up_sf;          // [E][f/128][d/128][512] chunk layout (prefill)
-  uint8_t *down_codes, *down_scales, *down_sf;  // MXFP4 down: [E][d][f/2], [E][d][f/32], chunks
-  uint8_t* q2k_qs;     // Q2_K down: [E][d][f/4]   2-bit codes, 4 per byte
-  uint8_t* q2k_sc;     // [E][d][f/16]  sub-block scale bytes
-  uint32_t* q2k_dd;    // [E][d][f/256] (fp16 d | fp16 dmin << 16)
+  uint8_t* down_sf;                  // [E][d/128][f/128][512]
+  // Q2_K down, tile-major: one 3072-byte chunk per (expert, 128-row block,
+  // 64-weight K step): 128 x 16 B 2-bit codes | 128 x 4 sub-block scale bytes
+  // | 128 x (fp16 d | fp16 dmin << 16) of the super-block the step lies in.
+  uint8_t* q2k;        // [E][d/128][f/64][3072]
 };
 
 }  // namespace ds4moe
@@ -87,7 +97,7 @@ namespace ds4moe {
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; none synchronises.
-cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
                               cudaStream_t st);
 cudaError_t launch_route_group(const ds4moe_layer* L, int T, cudaStream_t st);
 
@@ -102,6 +112,8 @@ cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaS
 // create-time repacking
 cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, cudaStream_t st);
 cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream_t st);
+cudaError_t launch_pack_rows(uint8_t* dst, int pitch, int64_t rows, const uint8_t* s0, int l0, const uint8_t* s1,
+                             int l1, const uint8_t* s2, int l2, const uint8_t* s3, int l3, cudaStream_t st);
 
 int decode_launches();
 int prefill_launches();

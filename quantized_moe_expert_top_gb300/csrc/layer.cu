@@ -33,15 +33,45 @@ __global__ void repack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __res
   }
 }
 
-// Q2_K super-blocks [E][d][f/256][84] -> split arrays with aligned rows:
-// qs [E][d][f/4], sc [E][d][f/16], dd [E][d][f/256] (d | dmin << 16).
-__global__ void repack_q2k_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ qs, uint8_t* __restrict__ sc,
-                                  uint32_t* __restrict__ dd, size_t nblocks) {
-  for (size_t b = (size_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += (size_t)gridDim.x * blockDim.x) {
-    const uint8_t* s = src + b * 84;
-    for (int i = 0; i < 16; ++i) sc[b * 16 + i] = s[i];
-    for (int i = 0; i < 64; ++i) qs[b * 64 + i] = s[16 + i];
-    dd[b] = (uint32_t)s[80] | ((uint32_t)s[81] << 8) | ((uint32_t)s[82] << 16) | ((uint32_t)s[83] << 24);
+// Interleaved rows: row r of dst (pitch bytes) = segment 0 row r (l0 bytes) |
+// segment 1 row r (l1) | ... (segments with l = 0 are skipped; lengths and
+// pitch are multiples of 4 bytes, sources 4-byte aligned).
+__global__ void pack_rows_kernel(uint8_t* __restrict__ dst, int pitch, int64_t rows, const uint8_t* __restrict__ s0,
+                                 int l0, const uint8_t* __restrict__ s1, int l1, const uint8_t* __restrict__ s2,
+                                 int l2, const uint8_t* __restrict__ s3, int l3) {
+  const uint8_t* src[4] = {s0, s1, s2, s3};
+  const int len[4] = {l0, l1, l2, l3};
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    uint32_t* d = reinterpret_cast<uint32_t*>(dst + r * pitch);
+    int off = 0;
+    for (int s = 0; s < 4; ++s) {
+      if (len[s] == 0) continue;
+      const uint32_t* sp = reinterpret_cast<const uint32_t*>(src[s] + r * len[s]);
+      for (int i = threadIdx.x; i < len[s] / 4; i += blockDim.x) d[off / 4 + i] = sp[i];
+      off += len[s];
+    }
+    for (int i = off / 4 + threadIdx.x; i < pitch / 4; i += blockDim.x) d[i] = 0u;
+  }
+}
+
+// Q2_K super-blocks [E][d][f/256][84] -> tile-major chunks [E][d/128][f/64]
+// of 3072 bytes: for row r of the 128-row block and K step kb (64 weights,
+// quarter kb % 4 of super-block kb / 4): bytes 16r.. the 16 code bytes of that
+// quarter, 2048 + 4r.. its 4 sub-block scale bytes, 2560 + 4r.. d | dmin.
+__global__ void repack_q2k_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int d, int f) {
+  const int KB = f / 64, nsb = f / 256;
+  const size_t total = (size_t)E * d * KB;  // one thread per (expert, row, K step)
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int kb = (int)(i % KB);
+    const size_t er = i / KB;
+    const int row = (int)(er % d);
+    const int e = (int)(er / d);
+    const uint8_t* blk = src + (((size_t)e * d + row) * nsb + kb / 4) * 84;
+    const int q4 = kb % 4, r = row % 128;
+    uint8_t* ch = dst + (((size_t)e * (d / 128) + row / 128) * KB + kb) * kQ2kChunk;
+    for (int b = 0; b < 16; ++b) ch[16 * r + b] = blk[16 + 16 * q4 + b];
+    for (int b = 0; b < 4; ++b) ch[2048 + 4 * r + b] = blk[4 * q4 + b];
+    for (int b = 0; b < 4; ++b) ch[2560 + 4 * r + b] = blk[80 + b];
   }
 }
 
@@ -184,6 +214,8 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   const int Tdec = (cfg->force_path == DS4MOE_PATH_DECODE || Tm < cfg->decode_max_tokens) ? Tm
                                                                                           : cfg->decode_max_tokens;
   L->s.pad_rows_max = pad_rows;
+  L->w.pitch_gu = (d + d / 16 + 31) / 32 * 32;
+  L->w.pitch_dn = (f / 2 + f / 32 + 31) / 32 * 32;
 
 #define TRY(x)                 \
   do {                         \
@@ -193,22 +225,16 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   {
     Weights& w = L->w;
     Scratch& s = L->s;
-    TRY(alloc(L, &w.gate_codes, gu_codes));
-    TRY(alloc(L, &w.up_codes, gu_codes));
-    TRY(alloc(L, &w.gate_scales, gu_scales));
-    TRY(alloc(L, &w.up_scales, gu_scales));
+    TRY(alloc(L, &w.gu, (size_t)E * f * w.pitch_gu));
     if (need_pre) {
       TRY(alloc(L, &w.gate_sf, gu_scales));
       TRY(alloc(L, &w.up_sf, gu_scales));
     }
     if (!q2k) {
-      TRY(alloc(L, &w.down_codes, dn_codes));
-      TRY(alloc(L, &w.down_scales, dn_scales));
+      TRY(alloc(L, &w.dn, (size_t)E * d * w.pitch_dn));
       if (need_pre) TRY(alloc(L, &w.down_sf, dn_scales));
     } else {
-      TRY(alloc(L, &w.q2k_qs, (size_t)E * d * (f / 4)));
-      TRY(alloc(L, &w.q2k_sc, (size_t)E * d * (f / 16)));
-      TRY(alloc(L, &w.q2k_dd, (size_t)E * d * (f / 256) * 4));
+      TRY(alloc(L, &w.q2k, (size_t)E * (d / 128) * (f / 64) * kQ2kChunk));
     }
     TRY(alloc(L, &s.topk_idx, pairs * 4));
     TRY(alloc(L, &s.topk_w, pairs * 4));
@@ -221,7 +247,11 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
     TRY(alloc(L, &s.pad_inv, pairs * 4));
     TRY(alloc(L, &s.pad_pair, (size_t)pad_rows * 4));
     TRY(alloc(L, &s.touched, (size_t)(E + 1) * 4));
-    if (need_dec) TRY(alloc(L, &s.h_dec, (size_t)Tdec * k * f * 4));
+    if (need_dec) {
+      TRY(alloc(L, &s.h_dec, (size_t)Tdec * k * f * 4));
+      TRY(alloc(L, &s.xh, (size_t)Tdec * d * 2));
+      TRY(alloc(L, &s.xsig, (size_t)Tdec * 4));
+    }
     if (need_pre) {
       TRY(alloc(L, &s.xq, (size_t)pad_rows * d));
       TRY(alloc(L, &s.xsf, (size_t)pad_rows * d / 32));
@@ -251,22 +281,23 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
         ok = ok && cudaMemset(s.hsf, 127, (size_t)pad_rows * f / 32) == cudaSuccess;
       }
     }
-    ok = ok && cudaMemcpy(w.gate_codes, wts->gate_codes, gu_codes, cudaMemcpyDeviceToDevice) == cudaSuccess;
-    ok = ok && cudaMemcpy(w.up_codes, wts->up_codes, gu_codes, cudaMemcpyDeviceToDevice) == cudaSuccess;
-    ok = ok && cudaMemcpy(w.gate_scales, wts->gate_scales, gu_scales, cudaMemcpyDeviceToDevice) == cudaSuccess;
-    ok = ok && cudaMemcpy(w.up_scales, wts->up_scales, gu_scales, cudaMemcpyDeviceToDevice) == cudaSuccess;
-    if (!q2k) {
-      ok = ok && cudaMemcpy(w.down_codes, wts->down_codes, dn_codes, cudaMemcpyDeviceToDevice) == cudaSuccess;
-      ok = ok && cudaMemcpy(w.down_scales, wts->down_scales, dn_scales, cudaMemcpyDeviceToDevice) == cudaSuccess;
-    }
     if (!ok) {
       rc = DS4MOE_ERR_CUDA;
       goto fail;
     }
+    (void)gu_codes;
+    (void)dn_codes;
+    if (launch_pack_rows(w.gu, w.pitch_gu, (int64_t)E * f, wts->gate_codes, d / 2, wts->up_codes, d / 2,
+                         wts->gate_scales, d / 32, wts->up_scales, d / 32, st) != cudaSuccess ||
+        (!q2k && launch_pack_rows(w.dn, w.pitch_dn, (int64_t)E * d, wts->down_codes, f / 2, wts->down_scales,
+                                  f / 32, nullptr, 0, nullptr, 0, st) != cudaSuccess)) {
+      rc = DS4MOE_ERR_CUDA;
+      goto fail;
+    }
     if (need_pre) {
-      if (launch_repack_sf(w.gate_scales, w.gate_sf, E, f, d, st) != cudaSuccess ||
-          launch_repack_sf(w.up_scales, w.up_sf, E, f, d, st) != cudaSuccess ||
-          (!q2k && launch_repack_sf(w.down_scales, w.down_sf, E, d, f, st) != cudaSuccess)) {
+      if (launch_repack_sf(wts->gate_scales, w.gate_sf, E, f, d, st) != cudaSuccess ||
+          launch_repack_sf(wts->up_scales, w.up_sf, E, f, d, st) != cudaSuccess ||
+          (!q2k && launch_repack_sf(wts->down_scales, w.down_sf, E, d, f, st) != cudaSuccess)) {
         rc = DS4MOE_ERR_CUDA;
         goto fail;
       }
@@ -276,15 +307,15 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       goto fail;
     }
     if (need_pre) {
-      bool tm_ok = encode_2d(&L->tm_gate, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gate_codes, d, (uint64_t)E * f,
-                             d / 2, 128, 128) &&
-                   encode_2d(&L->tm_up, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.up_codes, d, (uint64_t)E * f, d / 2,
-                             128, 128) &&
+      bool tm_ok = encode_2d(&L->tm_gate, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu, d, (uint64_t)E * f,
+                             w.pitch_gu, 128, 128) &&
+                   encode_2d(&L->tm_up, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu + d / 2, d, (uint64_t)E * f,
+                             w.pitch_gu, 128, 128) &&
                    encode_2d(&L->tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, 32);
       if (!q2k) {
         tm_ok = tm_ok &&
-                encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.down_codes, f, (uint64_t)E * d,
-                          f / 2, 128, 128) &&
+                encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn, f, (uint64_t)E * d,
+                          w.pitch_dn, 128, 128) &&
                 encode_2d(&L->tm_hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, 32);
       } else {
         tm_ok = tm_ok && encode_2d(&L->tm_h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.h16, f, pad_rows, (uint64_t)f * 2,
@@ -348,7 +379,7 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   cudaError_t e = L->timing ? cudaEventRecord(L->ev[0], st) : cudaSuccess;
   nk = 1;
   if (e == cudaSuccess)
-    e = mark(launch_route_topk(logits, T, L->cfg.n_experts, L->cfg.top_k, L->s.topk_idx, L->s.topk_w, st));
+    e = mark(launch_route_topk(L, logits, x, path == DS4MOE_PATH_DECODE, T, st));
   if (e == cudaSuccess) e = mark(launch_route_group(L, T, st));
   if (path == DS4MOE_PATH_DECODE) {
     if (e == cudaSuccess) e = mark(launch_decode_gateup(L, x, out, T, st));
@@ -487,10 +518,17 @@ cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_rows(uint8_t* dst, int pitch, int64_t rows, const uint8_t* s0, int l0, const uint8_t* s1,
+                             int l1, const uint8_t* s2, int l2, const uint8_t* s3, int l3, cudaStream_t st) {
+  const int grid = (int)(rows < 65536 ? rows : 65536);
+  pack_rows_kernel<<<grid, 128, 0, st>>>(dst, pitch, rows, s0, l0, s1, l1, s2, l2, s3, l3);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream_t st) {
-  const size_t nb = (size_t)L->cfg.n_experts * L->cfg.d_model * (L->cfg.d_ff / 256);
-  const int grid = (int)((nb + 255) / 256 < 65536 ? (nb + 255) / 256 : 65536);
-  repack_q2k_kernel<<<grid, 256, 0, st>>>(blocks, L->w.q2k_qs, L->w.q2k_sc, L->w.q2k_dd, nb);
+  const size_t n = (size_t)L->cfg.n_experts * L->cfg.d_model * (L->cfg.d_ff / 64);
+  const int grid = (int)((n + 255) / 256 < 65536 ? (n + 255) / 256 : 65536);
+  repack_q2k_kernel<<<grid, 256, 0, st>>>(blocks, L->w.q2k, L->cfg.n_experts, L->cfg.d_model, L->cfg.d_ff);
   return cudaGetLastError();
 }
 

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
 }
 
 // --------------------------------------------------------------- GEMM
-enum class Mode { GateUp, Down };
+enum class Mode { GateUp, Down, DownQ2K };
 
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: A/B formats
 // (E4M3 = 0, E2M1 = 5), K-major A and B, N >> 3, E8M0 scales, M >> 4, and the
@@ -100,43 +100,72 @@ __device__ __forceinline__ uint32_t idesc_mx(int N, uint32_t sf_id) {
          ((uint32_t)(kBM >> 4) << 24) | (sf_id << 29);
 }
 
+// Instruction descriptor, kind::f16: f16 A and B, f32 D, K-major, N >> 3, M >> 4.
+__device__ __forceinline__ uint32_t idesc_f16(int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+// Tensor-memory plan (512 columns): accumulator buffer(s) at columns 0 and
+// 256, scale-factor slots from column 448 up.  One pipeline stage covers kKs
+// contraction elements (128 bytes of every operand row).
 template <Mode M>
 struct Cfg;
 template <>
 struct Cfg<Mode::GateUp> {
-  static constexpr int kNumA = 2;
-  static constexpr int kNMax = 192;
-  static constexpr int kStages = 3;
-  static constexpr int kAccCol2 = 256;  // up accumulator column
-  static constexpr int kSfBase = 448;   // scale-factor slots (16 columns each)
-  static constexpr int kSfSlot = 16;
-  static constexpr int kSfSlots = 4;
+  static constexpr int kNumA = 2;       // gate and up tiles
+  static constexpr int kNMax = 160;     // token columns per chunk
+  static constexpr int kStages = 4;
+  static constexpr int kAccBufs = 1;    // G at column 0, U at column 256
+  static constexpr int kSfSlot = 16;    // SFA gate 4 + SFA up 4 + SFB 8 columns
+  static constexpr int kKs = 128;       // E2M1 / E4M3 elements per stage
+  static constexpr int kDeqWarps = 0;
 };
 template <>
 struct Cfg<Mode::Down> {
   static constexpr int kNumA = 1;
-  static constexpr int kNMax = 256;
+  static constexpr int kNMax = 192;
   static constexpr int kStages = 4;
-  static constexpr int kAccCol2 = 0;
-  static constexpr int kSfBase = 256;
-  static constexpr int kSfSlot = 12;
-  static constexpr int kSfSlots = 4;
+  static constexpr int kAccBufs = 2;    // double-buffered: columns 0 and 256
+  static constexpr int kSfSlot = 12;    // SFA 4 + SFB 8 columns
+  static constexpr int kKs = 128;
+  static constexpr int kDeqWarps = 0;
 };
-
-static_assert(Cfg<Mode::GateUp>::kSfSlots >= Cfg<Mode::GateUp>::kStages, "scale slots");
-static_assert(Cfg<Mode::Down>::kSfSlots >= Cfg<Mode::Down>::kStages, "scale slots");
+template <>
+struct Cfg<Mode::DownQ2K> {
+  static constexpr int kNumA = 1;
+  static constexpr int kNMax = 192;
+  static constexpr int kStages = 4;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kSfSlot = 0;
+  static constexpr int kKs = 64;        // fp16 elements per stage
+  static constexpr int kDeqWarps = 4;   // Q2_K -> fp16 producers, one weight row per thread
+};
+constexpr int kAccCol2 = 256;
+constexpr int kSfBase = 448;
+constexpr int kSfSlots = 4;
+constexpr int kEpiWarps = 8;           // two per tensor-memory lane quarter
+template <Mode M>
+constexpr int threads_of() { return 64 + 32 * kEpiWarps + 32 * Cfg<M>::kDeqWarps; }
+constexpr int kPrefetchStages = 8;     // weight tiles prefetched into L2 ahead of their load
+static_assert(kSfSlots >= Cfg<Mode::GateUp>::kStages && kSfSlots >= Cfg<Mode::Down>::kStages, "scale slots");
+static_assert(kSfBase + kSfSlots * Cfg<Mode::GateUp>::kSfSlot <= 512, "tmem");
+static_assert(Cfg<Mode::GateUp>::kNMax <= 256 && kAccCol2 + Cfg<Mode::GateUp>::kNMax <= kSfBase, "tmem");
+static_assert(kAccCol2 + Cfg<Mode::Down>::kNMax <= kSfBase, "tmem");
 
 template <Mode M>
 struct Smem {
-  static constexpr int kA = kBM * kBK;                    // 16 KB per weight tile
-  static constexpr int kB = Cfg<M>::kNMax * kBK;           // token tile
-  static constexpr int kSf = (kSfChunk * (Cfg<M>::kNumA + 2) + 1023) / 1024 * 1024;
+  static constexpr int kA = kBM * 128;                    // 16 KB per weight tile (128-byte rows)
+  static constexpr int kB = Cfg<M>::kNMax * 128;           // token tile
+  static constexpr int kSf = M == Mode::DownQ2K ? 4096    // Q2_K chunk
+                                                : (kSfChunk * (Cfg<M>::kNumA + 2) + 1023) / 1024 * 1024;
   static constexpr int kStage = Cfg<M>::kNumA * kA + kB + kSf;
-  static constexpr int kBarOff = Cfg<M>::kStages * kStage;
-  static constexpr int kTotal = kBarOff + 256 + 1024;     // + barriers, + alignment slack
+  static constexpr int kColOff = Cfg<M>::kStages * kStage;  // down: per-column (token, weight) table
+  static constexpr int kBarOff = kColOff + Cfg<M>::kNMax * 8;
+  static constexpr int kTotal = kBarOff + 256 + 1024;       // + barriers, + alignment slack
 };
 static_assert(Smem<Mode::GateUp>::kStage % 1024 == 0, "stage alignment");
 static_assert(Smem<Mode::Down>::kStage % 1024 == 0, "stage alignment");
+static_assert(Smem<Mode::DownQ2K>::kStage % 1024 == 0, "stage alignment");
 
 struct GemmArgs {
   // weights
@@ -152,6 +181,7 @@ struct GemmArgs {
   const int32_t* pad_pair;
   const float* topk_w;
   int E, k, d, f;
+  const uint8_t* q2k;  // Q2_K down: tile-major chunks
   // outputs
   uint8_t* hq;    // gate/up: MXFP8 h codes [rows][f]
   uint8_t* hsf;   // gate/up: h scales (chunk layout)
@@ -162,9 +192,9 @@ struct GemmArgs {
   int debug_fault;
 };
 
-// Work unit sequence shared by the three roles: units u = (expert, 128-row
-// block), expert-major; each unit's tokens split into chunks that start on a
-// 128-token boundary (one chunk when they fit in kNMax columns).
+// Work sequence shared by the roles: units u = (expert, 128-row block),
+// expert-major, strided over the CTAs; each unit's tokens split into chunks
+// that start on a 128-token boundary (one chunk when they fit in kNMax).
 struct UnitIter {
   int u, nunits, stride, mb_per_e;
   int e, mb, ne, t0, nch;
@@ -195,37 +225,62 @@ struct UnitIter {
   }
 };
 
+// The same sequence one pipeline stage at a time (the producer's L2 prefetch
+// cursor runs kPrefetchStages ahead of its load cursor).
+struct StageIter {
+  UnitIter it;
+  int kb, KB;
+  bool valid;
+  __device__ void start() {
+    kb = 0;
+    valid = it.first_chunk();
+  }
+  __device__ void next() {
+    if (!valid) return;
+    if (++kb < KB) return;
+    kb = 0;
+    valid = it.next();
+  }
+};
+
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 template <Mode M>
-__global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
-                                                              const __grid_constant__ CUtensorMap tm_a1,
-                                                              const __grid_constant__ CUtensorMap tm_b,
-                                                              const GemmArgs args) {
+__global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                                                                       const __grid_constant__ CUtensorMap tm_a1,
+                                                                       const __grid_constant__ CUtensorMap tm_b,
+                                                                       const GemmArgs args) {
   using C = Cfg<M>;
   using S = Smem<M>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  int32_t* col_tok = reinterpret_cast<int32_t*>(smem + S::kColOff);
+  float* col_w = reinterpret_cast<float*>(col_tok + C::kNMax);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);  // TMA bytes of a stage
   uint64_t* empty = full + C::kStages;
-  uint64_t* acc_full = empty + C::kStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* afull = empty + C::kStages;      // Q2_K: dequantised A tile written
+  uint64_t* acc_full = afull + C::kStages;   // [kAccBufs]
+  uint64_t* acc_empty = acc_full + 2;        // [kAccBufs]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_ok = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mb_per_e = args.rows_per_expert / kBM;
   const int nunits = args.E * mb_per_e;
-  const int KB = args.K / kBK;
+  const int KB = args.K / C::kKs;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&afull[s], C::kDeqWarps > 0 ? C::kDeqWarps : 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -245,54 +300,82 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
+      StageIter ld{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax},
+                   0, KB, false};
+      ld.start();
+      StageIter pf = ld;  // L2 prefetch cursor
+      auto prefetch = [&](const StageIter& p) {
+        const size_t tile = ((size_t)(p.it.e * mb_per_e + p.it.mb) * KB + p.kb);
+        if constexpr (M == Mode::DownQ2K) {
+          bulk_prefetch_l2(args.q2k + tile * kQ2kChunk, kQ2kChunk);
+        } else {
+          const int arow = p.it.e * args.rows_per_expert + p.it.mb * kBM;
+          tma_prefetch_2d(&tm_a0, p.kb * C::kKs, arow);
+          if (C::kNumA > 1) tma_prefetch_2d(&tm_a1, p.kb * C::kKs, arow);
+          bulk_prefetch_l2(args.sfa0 + tile * kSfChunk, kSfChunk);
+          if (C::kNumA > 1) bulk_prefetch_l2(args.sfa1 + tile * kSfChunk, kSfChunk);
+        }
+      };
+      for (int i = 0; i < kPrefetchStages && pf.valid; ++i) {
+        prefetch(pf);
+        pf.next();
+      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
-      bool ok = true, fault_pending = args.debug_fault && blockIdx.x == 0;
-      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
-        const int N = round16(it.nch);
+      bool fault_pending = args.debug_fault && blockIdx.x == 0;
+      while (ld.valid) {
+        const int N = round16(ld.it.nch);
         const int nb = (N + 31) / 32, nsf = (N + 127) / 128;
-        const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
-        const int arow = it.e * args.rows_per_expert + it.mb * kBM;
+        const int prow = __ldg(args.pad_offsets + ld.it.e) + ld.it.t0;
+        const int arow = ld.it.e * args.rows_per_expert + ld.it.mb * kBM;
         // A 4-bit unpacking load counts its packed global bytes (half the
         // 16 KB it writes to shared memory).
-        const uint32_t bytes = (uint32_t)(C::kNumA * S::kA / 2 + nb * 32 * kBK + (C::kNumA + nsf) * kSfChunk);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
-            report_timeout(args.status, kWhereProducerEmpty);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          uint8_t* st = smem + stage * S::kStage;
-          uint8_t* sa0 = st;
-          uint8_t* sa1 = st + S::kA;
-          uint8_t* sb = st + C::kNumA * S::kA;
-          uint8_t* ssf = sb + S::kB;
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          if (fault_pending) {
-            fault_pending = false;  // test-only: drop this stage's loads
-          } else {
-            tma_load_2d(sa0, &tm_a0, &full[stage], kb * kBK, arow);
-            if (C::kNumA > 1) tma_load_2d(sa1, &tm_a1, &full[stage], kb * kBK, arow);
-            for (int i = 0; i < nb; ++i) tma_load_2d(sb + i * 32 * kBK, &tm_b, &full[stage], kb * kBK, prow + 32 * i);
-            const size_t sfa_off = ((size_t)(it.e * mb_per_e + it.mb) * KB + kb) * kSfChunk;
-            bulk_load(ssf, args.sfa0 + sfa_off, kSfChunk, &full[stage]);
-            if (C::kNumA > 1) bulk_load(ssf + kSfChunk, args.sfa1 + sfa_off, kSfChunk, &full[stage]);
-            for (int i = 0; i < nsf; ++i)
-              bulk_load(ssf + (C::kNumA + i) * kSfChunk, args.sfb + ((size_t)(prow / 128 + i) * KB + kb) * kSfChunk,
-                        kSfChunk, &full[stage]);
-          }
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        const uint32_t bytes = M == Mode::DownQ2K
+                                   ? (uint32_t)(nb * 32 * 128 + kQ2kChunk)
+                                   : (uint32_t)(C::kNumA * S::kA / 2 + nb * 32 * 128 + (C::kNumA + nsf) * kSfChunk);
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
+          report_timeout(args.status, kWhereProducerEmpty);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + stage * S::kStage;
+        uint8_t* sa0 = st;
+        uint8_t* sa1 = st + S::kA;
+        uint8_t* sb = st + C::kNumA * S::kA;
+        uint8_t* ssf = sb + S::kB;
+        (void)sa1;
+        const int kb = ld.kb;
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        const size_t tile = ((size_t)(ld.it.e * mb_per_e + ld.it.mb) * KB + kb);
+        if (fault_pending) {
+          fault_pending = false;  // test-only: drop this stage's loads
+        } else if constexpr (M == Mode::DownQ2K) {
+          for (int i = 0; i < nb; ++i) tma_load_2d(sb + i * 32 * 128, &tm_b, &full[stage], kb * C::kKs, prow + 32 * i);
+          bulk_load(ssf, args.q2k + tile * kQ2kChunk, kQ2kChunk, &full[stage]);
+        } else {
+          tma_load_2d(sa0, &tm_a0, &full[stage], kb * C::kKs, arow);
+          if (C::kNumA > 1) tma_load_2d(sa1, &tm_a1, &full[stage], kb * C::kKs, arow);
+          for (int i = 0; i < nb; ++i) tma_load_2d(sb + i * 32 * 128, &tm_b, &full[stage], kb * C::kKs, prow + 32 * i);
+          bulk_load(ssf, args.sfa0 + tile * kSfChunk, kSfChunk, &full[stage]);
+          if (C::kNumA > 1) bulk_load(ssf + kSfChunk, args.sfa1 + tile * kSfChunk, kSfChunk, &full[stage]);
+          for (int i = 0; i < nsf; ++i)
+            bulk_load(ssf + (C::kNumA + i) * kSfChunk, args.sfb + ((size_t)(prow / 128 + i) * KB + kb) * kSfChunk,
+                      kSfChunk, &full[stage]);
+        }
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        ld.next();
+        if (pf.valid) {
+          prefetch(pf);
+          pf.next();
         }
       }
-      if (!ok) {
+      if (*abort_flag) {
         // drain: every issued stage's copies must land before the CTA exits
         for (int s = 0; s < C::kStages; ++s)
           if ((issued_mask >> s) & 1u) {
@@ -307,19 +390,21 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
     if (lane == 0) {
       UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0, acc_phase = 0;  // acc_phase bit b: phase of accumulator buffer b
       uint32_t sf_seq = 0;  // running stage count; slot = sf_seq % kSfSlots (kSfSlots >= kStages)
+      int chunk = 0;
       bool ok = true;
-      const uint32_t sf_tmem = tmem + C::kSfBase;
-      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
+      for (bool more = it.first_chunk(); more && ok; more = it.next(), ++chunk) {
         const int N = round16(it.nch);
         const int nsf = (N + 127) / 128;
-        if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, args.budget_ns, abort_flag)) {
+        const int buf = chunk % C::kAccBufs;
+        const uint32_t acc0 = tmem + (uint32_t)(buf * kAccCol2);
+        if (!mbar_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
           report_timeout(args.status, kWhereMmaAccEmpty);
           *abort_flag = 1;
           break;
         }
-        acc_phase ^= 1u;
+        acc_phase ^= 1u << buf;
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag)) {
@@ -328,24 +413,41 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
             ok = false;
             break;
           }
+          if constexpr (M == Mode::DownQ2K) {  // the dequantised A tile is written by the dequant warps
+            if (!mbar_wait_bounded(&afull[stage], phase, args.budget_ns, abort_flag)) {
+              report_timeout(args.status, kWhereMmaFull);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
           uint8_t* st = smem + stage * S::kStage;
           const uint32_t a0 = smem_u32(st), a1 = smem_u32(st + S::kA);
           const uint32_t b = smem_u32(st + C::kNumA * S::kA);
           const uint32_t ssf = b + S::kB;
-          const uint32_t slot = sf_tmem + (sf_seq++ % C::kSfSlots) * C::kSfSlot;
-          // scale factors -> tensor memory: A chunk(s) at slot+0 (+4), B chunks after
-          for (int i = 0; i < C::kNumA + nsf; ++i)
-            tc_cp_32x128b_warpx4(slot + 4 * i, smem_desc(ssf + i * kSfChunk, 0, 128, 0));
+          (void)a1;
+          if constexpr (M == Mode::DownQ2K) {
+            const uint32_t idesc = idesc_f16(N);
 #pragma unroll
-          for (int j = 0; j < kBK / 32; ++j) {
-            const uint32_t idesc = idesc_mx(N, (uint32_t)j);
-            const uint64_t bd = smem_desc(b + 32 * j, 16, 1024, 2);
-            const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-            mma_mxf8f6f4(tmem, smem_desc(a0 + 32 * j, 16, 1024, 2), bd, idesc, slot, slot + 4 * C::kNumA, accum);
-            if (C::kNumA > 1)
-              mma_mxf8f6f4(tmem + C::kAccCol2, smem_desc(a1 + 32 * j, 16, 1024, 2), bd, idesc, slot + 4,
-                           slot + 4 * C::kNumA, accum);
+            for (int j = 0; j < 4; ++j)  // K = 16 fp16 (32 bytes) per instruction
+              mma_f16(acc0, smem_desc(a0 + 32 * j, 16, 1024, 2), smem_desc(b + 32 * j, 16, 1024, 2), idesc,
+                      (kb > 0 || j > 0) ? 1u : 0u);
+          } else {
+            const uint32_t slot = tmem + kSfBase + (sf_seq++ % kSfSlots) * C::kSfSlot;
+            // scale factors -> tensor memory: A chunk(s) at slot+0 (+4), B chunks after
+            for (int i = 0; i < C::kNumA + nsf; ++i)
+              tc_cp_32x128b_warpx4(slot + 4 * i, smem_desc(ssf + i * kSfChunk, 0, 128, 0));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // K = 32 (32 bytes) per instruction
+              const uint32_t idesc = idesc_mx(N, (uint32_t)j);
+              const uint64_t bd = smem_desc(b + 32 * j, 16, 1024, 2);
+              const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+              mma_mxf8f6f4(acc0, smem_desc(a0 + 32 * j, 16, 1024, 2), bd, idesc, slot, slot + 4 * C::kNumA, accum);
+              if (C::kNumA > 1)
+                mma_mxf8f6f4(acc0 + kAccCol2, smem_desc(a1 + 32 * j, 16, 1024, 2), bd, idesc, slot + 4,
+                             slot + 4 * C::kNumA, accum);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == C::kStages) {
@@ -354,7 +456,7 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
           }
         }
         if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit(&acc_full[buf]);
       }
       // drain all MMAs this thread issued before tensor memory is freed
       tc_commit(drain);
@@ -362,52 +464,150 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
       mbar_wait_bounded(drain, 0, args.budget_ns, &never);
     }
     __syncwarp();
+  } else if (warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------------------ Q2_K dequant
+    if constexpr (M == Mode::DownQ2K) {
+      const int r = (warp - 2 - kEpiWarps) * 32 + lane;  // weight row of the 128-row tile
+      StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax},
+                   0, KB, false};
+      sq.start();
+      int stage = 0;
+      uint32_t phase = 0;
+      const __half2 k1024 = __float2half2_rn(1024.f);
+      while (sq.valid) {
+        uint32_t got = 0;
+        if (lane == 0) got = mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag) ? 1u : 0u;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          if (lane == 0) {
+            report_timeout(args.status, kWhereMmaFull);
+            *abort_flag = 1;
+          }
+          break;
+        }
+        uint8_t* st = smem + stage * S::kStage;
+        const uint8_t* ch = st + S::kA + S::kB;
+        const uint4 qv = *reinterpret_cast<const uint4*>(ch + 16 * r);
+        const uint32_t scw = *reinterpret_cast<const uint32_t*>(ch + 2048 + 4 * r);
+        const uint32_t ddw = *reinterpret_cast<const uint32_t*>(ch + 2560 + 4 * r);
+        const float dd = __half2float(__ushort_as_half((unsigned short)(ddw & 0xFFFFu)));
+        const float dm = __half2float(__ushort_as_half((unsigned short)(ddw >> 16)));
+        const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+        uint8_t* arow = st + r * 128;
+#pragma unroll
+        for (int sb = 0; sb < 4; ++sb) {  // sub-block sb = weights 16 sb .. 16 sb + 15 of the step
+          const uint32_t scb = (scw >> (8 * sb)) & 0xFFu;
+          const __half2 a2 = __float2half2_rn(dd * (float)(scb & 15u));
+          const __half2 nb2 = __float2half2_rn(-dm * (float)(scb >> 4));
+          uint32_t P[8];  // P[n] = {w_n, w_(n+8)}: 2-bit codes 16 bits apart in the word
+#pragma unroll
+          for (int n = 0; n < 8; ++n) {
+            const uint32_t v = ((words[sb] >> (2 * n)) & 0x00030003u) | 0x64006400u;  // f16 1024 + q
+            const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&v), k1024);
+            const __half2 w2 = __hfma2(q2, a2, nb2);
+            P[n] = *reinterpret_cast<const uint32_t*>(&w2);
+          }
+          const uint4 lo = make_uint4(__byte_perm(P[0], P[1], 0x5410), __byte_perm(P[2], P[3], 0x5410),
+                                      __byte_perm(P[4], P[5], 0x5410), __byte_perm(P[6], P[7], 0x5410));
+          const uint4 hi = make_uint4(__byte_perm(P[0], P[1], 0x7632), __byte_perm(P[2], P[3], 0x7632),
+                                      __byte_perm(P[4], P[5], 0x7632), __byte_perm(P[6], P[7], 0x7632));
+          // 16-byte chunks 2 sb and 2 sb + 1 of the row, 128-byte swizzle
+          *reinterpret_cast<uint4*>(arow + (((2 * sb) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(arow + (((2 * sb + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        sq.next();
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    const int q = warp & 3;             // tensor-memory lane quarter this warp may access
+    const int half = (warp - 2) >> 2;   // which half of the 16-column chunks
+    const int etid = threadIdx.x - 64;  // 0..255 among the epilogue warps
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
     uint32_t acc_phase = 0;
-    for (bool more = it.first_chunk(); more; more = it.next()) {
-      uint32_t got = 0;
-      if (lane == 0) got = mbar_wait_bounded(acc_full, acc_phase, args.budget_ns, abort_flag) ? 1u : 0u;
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) {
-        if (lane == 0) {
-          report_timeout(args.status, kWhereEpiAccFull);
-          *abort_flag = 1;
-        }
-        break;
-      }
-      acc_phase ^= 1u;
-      tc_fence_after();
+    int chunk = 0;
+    for (bool more = it.first_chunk(); more; more = it.next(), ++chunk) {
       const int N = round16(it.nch);
       const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+      const int buf = chunk % C::kAccBufs;
+      uint32_t got = 0;
+      if (M != Mode::GateUp) {
+        // Per-column token and routing weight, loaded while the MMAs run.  One
+        // thread takes the accumulator wait and publishes the outcome, so all
+        // epilogue warps leave the loop together (the named barriers need
+        // every one of them).
+        named_bar_sync(1, 32 * kEpiWarps);  // previous chunk's table no longer read
+        for (int c = etid; c < it.nch; c += 32 * kEpiWarps) {
+          const int pair = __ldg(args.pad_pair + prow + c);
+          col_tok[c] = pair / args.k;
+          col_w[c] = __ldg(args.topk_w + pair);
+        }
+        if (etid == 0) {
+          const bool ok = mbar_wait_bounded(&acc_full[buf], (acc_phase >> buf) & 1u, args.budget_ns, abort_flag);
+          *epi_ok = ok ? 1 : 0;
+          if (!ok) {
+            report_timeout(args.status, kWhereEpiAccFull);
+            *abort_flag = 1;
+          }
+        }
+        named_bar_sync(1, 32 * kEpiWarps);
+        got = (uint32_t)*epi_ok;
+        if (!got) break;
+      } else {
+        if (lane == 0)
+          got = mbar_wait_bounded(&acc_full[buf], (acc_phase >> buf) & 1u, args.budget_ns, abort_flag) ? 1u : 0u;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          if (lane == 0) {
+            report_timeout(args.status, kWhereEpiAccFull);
+            *abort_flag = 1;
+          }
+          break;
+        }
+      }
+      acc_phase ^= 1u << buf;
+      tc_fence_after();
+      const uint32_t acc0 = tmem + (uint32_t)(buf * kAccCol2) + lane_base;
       const int unit_row = it.mb * kBM + q * 32 + lane;  // row of this lane inside the expert
-      for (int c0 = 0; c0 < N; c0 += 16) {
+      for (int c0 = half * 16; c0 < N; c0 += 32) {
         uint32_t r0[16];
-        tmem_ld_32x32b_x16(tmem + lane_base + (uint32_t)c0, r0);
+        tmem_ld_32x32b_x16(acc0 + (uint32_t)c0, r0);
         if (M == Mode::GateUp) {
           uint32_t r1[16];
-          tmem_ld_32x32b_x16(tmem + lane_base + (uint32_t)(C::kAccCol2 + c0), r1);
+          tmem_ld_32x32b_x16(acc0 + (uint32_t)(kAccCol2 + c0), r1);
           tmem_ld_wait();
           const int i = unit_row;  // feature index in [0, f)
+          float h[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            const int col = c0 + jj;
             const float g = __uint_as_float(r0[jj]), u = __uint_as_float(r1[jj]);
-            const float h = g / (1.f + expf(-g)) * u;
-            if (col < it.nch) {
-              const size_t row = (size_t)(prow + col);
-              if (args.h16 != nullptr) {
-                args.h16[row * args.f + i] = __float2half_rn(h);
-              } else {
-                const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
-                const float amax = __uint_as_float(amax_bits);
+            h[jj] = __fdividef(g, 1.f + __expf(-g)) * u;
+          }
+          if (args.h16 != nullptr) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (c0 + jj < it.nch) args.h16[(size_t)(prow + c0 + jj) * args.f + i] = __float2half_rn(h[jj]);
+          } else {
+            uint32_t amax[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) amax[jj] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj])));
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = c0 + jj;
+              if (col < it.nch) {
+                const float a = __uint_as_float(amax[jj]);
                 int s = 0;
-                if (amax > 0.f) s = max(-127, min(127, floor_log2_f32(amax) - 8));
-                const uint8_t code = (uint8_t)(f32x2_to_e4m3x2(h * exp2i(-s), 0.f) & 0xFFu);
-                args.hq[row * args.f + i] = code;
+                if (a > 0.f) s = max(-127, min(127, floor_log2_f32(a) - 8));
+                const size_t row = (size_t)(prow + col);
+                args.hq[row * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
                 if (lane == 0) {
                   const int kblk = i / 32;
                   args.hsf[((row / 128) * (size_t)(args.f / 128) + kblk / 4) * kSfChunk + (row % 32) * 16 +
@@ -422,18 +622,14 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int col = c0 + jj;
-            if (col < it.nch) {
-              const int pair = __ldg(args.pad_pair + prow + col);
-              const int t = pair / args.k;
-              const float wv = __ldg(args.topk_w + pair);
-              red_add_f32(args.out + (size_t)t * args.d + m, wv * __uint_as_float(r0[jj]));
-            }
+            if (col < it.nch)
+              red_add_f32(args.out + (size_t)col_tok[col] * args.d + m, col_w[col] * __uint_as_float(r0[jj]));
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
 
@@ -454,7 +650,7 @@ cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a0, const CUte
   if (e != cudaSuccess) return e;
   const int units = args.E * (args.rows_per_expert / kBM);
   const int grid = units < L->num_sms ? units : L->num_sms;
-  grouped_gemm_kernel<M><<<grid, 192, Smem<M>::kTotal, st>>>(a0, a1, b, args);
+  grouped_gemm_kernel<M><<<grid, threads_of<M>(), Smem<M>::kTotal, st>>>(a0, a1, b, args);
   return cudaGetLastError();
 }
 
@@ -511,8 +707,14 @@ cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStrea
 }
 
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
-  (void)L; (void)out; (void)T; (void)st;
-  return cudaErrorNotSupported;
+  (void)T;
+  GemmArgs a = base_args(L);
+  a.debug_fault = 0;
+  a.q2k = L->w.q2k;
+  a.rows_per_expert = L->cfg.d_model;
+  a.K = L->cfg.d_ff;
+  a.out = out;
+  return launch_gemm<Mode::DownQ2K>(L, L->tm_h16, L->tm_h16, L->tm_h16, a, st);
 }
 
 int prefill_launches() { return 5; }

@@ -19,11 +19,51 @@ constexpr int kMaxK = 8;
 
 // One warp per token.  Lane l holds logits l, l+32, ..., so a lane's own
 // entries are in increasing index order.
+//
+// For the decode path the same warp also prepares the token's activations: x
+// as f16 with a power-of-two prescale s (amax * 2^-s lands in [2^14, 2^15), so
+// every bf16 value is exact or below f16's subnormal floor), stored in the
+// piece-transposed order the decode GEMV reads (16-byte piece q of 32-element
+// block c at index q * d/32 + c), and 2^s in xsig[token].
+__device__ __forceinline__ void prepare_x_f16(const __nv_bfloat16* __restrict__ x, int token, int d,
+                                              uint4* __restrict__ xh, float* __restrict__ xsig, int lane) {
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)token * d);
+  const int npieces = d / 8, nblk = d / 32;
+  float amax = 0.f;
+  for (int i = lane; i < npieces; i += 32) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
+  }
+  amax = warp_max(amax);
+  const int s = f16_prescale_exp(amax);
+  const float inv = exp2i(-s);
+  if (lane == 0) xsig[token] = exp2i(s);
+  uint4* dst = xh + (size_t)token * npieces;
+  for (int i = lane; i < npieces; i += 32) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 hv =
+          __floats2half2_rn(__uint_as_float(wv[q] << 16) * inv, __uint_as_float(wv[q] & 0xFFFF0000u) * inv);
+      h[q] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    dst[(i & 3) * nblk + (i >> 2)] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int32_t* __restrict__ idx, float* __restrict__ w) {
+                                                         int32_t* __restrict__ idx, float* __restrict__ w,
+                                                         const __nv_bfloat16* __restrict__ x, int d,
+                                                         uint4* __restrict__ xh, float* __restrict__ xsig) {
   const int token = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
+  if (xh != nullptr) prepare_x_f16(x, token, d, xh, xsig, lane);
   const float* row = logits + (size_t)token * E;
 
   float v[kMaxE / 32];
@@ -199,10 +239,14 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
 
 }  // namespace
 
-cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w, cudaStream_t st) {
+cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
+                              cudaStream_t st) {
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
-  route_topk_kernel<<<blocks, 32 * warps_per_block, 0, st>>>(logits, T, E, k, idx, w);
+  route_topk_kernel<<<blocks, 32 * warps_per_block, 0, st>>>(
+      logits, T, L->cfg.n_experts, L->cfg.top_k, L->s.topk_idx, L->s.topk_w,
+      static_cast<const __nv_bfloat16*>(x), L->cfg.d_model, prep_x ? reinterpret_cast<uint4*>(L->s.xh) : nullptr,
+      L->s.xsig);
   return cudaGetLastError();
 }
 
