@@ -183,6 +183,27 @@ int ds4moe_set_kernel_timing(ds4moe_layer *layer, int enable);
 int ds4moe_kernel_times(ds4moe_layer *layer, float *ms, int max_n);
 const char *ds4moe_kernel_name(int path, int i);
 
+/* Routing alone (steps 1-2 above), allocating nothing.  The pages have no
+ * counterpart: this call exists for callers that cannot allocate device
+ * memory when they route, such as an engine whose memory plan is fixed at
+ * start-up, or a serving loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.  It needs no layer.  Its scratch is a file-scope device
+ * array sized for T*k <= 16384 and E <= 256 (about 390 KB), which every GPU
+ * that loads this library keeps until the process exits.
+ *   logits    device fp32 [T][E]
+ *   topk_idx  device int32 [T][k] out, topk_w device fp32 [T][k] out
+ *   offsets   device int32 [E+1] out, perm_tok device int32 [T*k] out
+ * Results equal those of ds4moe_forward's routing (see ds4moe_get_routing).
+ * Enqueued on `stream`; no host synchronisation.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current: make that first call before any stream capture.  Every call shares
+ * the one array and nothing in it needs to start at zero; calls whose GPU
+ * work overlaps (two streams, two host threads) race on it, so serialise them.
+ * Errors: INVALID_ARG (NULL or misaligned pointer, E or k out of range),
+ * TOO_MANY_TOKENS (T*k > 16384), CUDA. */
+int ds4moe_route_noalloc(const float *logits, int32_t T, int32_t E, int32_t k, int32_t *topk_idx,
+                         float *topk_w, int32_t *offsets, int32_t *perm_tok, ds4moe_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *ds4moe_status_string(int status);
 

@@ -6,7 +6,7 @@ Python sees a thin ctypes binding (:class:`Layer`); the compiled library is
 built in-tree by :func:`build`.
 """
 from ._binding import (  # noqa: F401
-    Config, Ds4moeError, Layer, WeightPtrs, default_config, header_functions, lib, status_string,
+    Config, Ds4moeError, Layer, WeightPtrs, default_config, header_functions, lib, route_noalloc, status_string,
     OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TOO_MANY_TOKENS, ERR_DEVICE_TIMEOUT,
     DOWN_MXFP4, DOWN_Q2K, PATH_AUTO, PATH_DECODE, PATH_PREFILL, LIB_PATH,
 )

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         L.ds4moe_kernel_name.restype = ctypes.c_char_p
         L.ds4moe_kernel_name.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.ds4moe_route_noalloc.restype = ctypes.c_int
+        L.ds4moe_route_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.ds4moe_status_string.restype = ctypes.c_char_p
         L.ds4moe_status_string.argtypes = [ctypes.c_int]
         L.ds4moe_destroy.restype = None
@@ -115,6 +117,23 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def route_noalloc(logits: torch.Tensor, k: int, stream=None) -> dict:
+    """Routing through ds4moe_route_noalloc (no device allocation inside the
+    library; the output tensors are allocated here by torch)."""
+    T, E = logits.shape
+    dev = logits.device
+    r = {"topk_idx": torch.empty(T, k, dtype=torch.int32, device=dev),
+         "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
+         "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+         "perm_tok": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)}
+    rc = lib().ds4moe_route_noalloc(_ptr(logits), T, E, k, _ptr(r["topk_idx"]), _ptr(r["topk_w"]),
+                                    _ptr(r["offsets"]), _ptr(r["perm_tok"]), _stream_handle(stream))
+    if rc != OK:
+        raise Ds4moeError(rc, "ds4moe_route_noalloc")
+    r["perm_tok"] = r["perm_tok"][:T * k]
+    return r
 
 
 class Layer:

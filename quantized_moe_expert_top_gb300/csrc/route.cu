@@ -11,6 +11,8 @@
 
 #include <math.h>
 
+#include <mutex>
+
 namespace ds4moe {
 namespace {
 
@@ -259,3 +261,80 @@ cudaError_t launch_route_group(const ds4moe_layer* L, int T, cudaStream_t st) {
 }
 
 }  // namespace ds4moe
+
+// ---------------------------------------------------------------------------
+// Routing without device allocation (ds4moe_route_noalloc).
+//
+// Some callers cannot call cudaMalloc when they route: an engine whose memory
+// plan is fixed at start-up and forbids later allocations, or a serving loop
+// that cannot pay cudaMalloc's implicit device synchronisation per batch.
+// This entry point runs the same two routing kernels with their scratch in a
+// file-scope device array instead of layer-owned buffers.  The array is
+// sized for T*k <= kNoAllocMaxPairs and E <= 256 and stays resident on every
+// GPU that loads this library until the process exits.
+namespace ds4moe {
+namespace {
+
+constexpr int kNoAllocMaxPairs = 16384;
+constexpr int kNoAllocMaxE = 256;
+// counts[E] | pad_offsets[E+1] | perm_slot[P] | inv[P] | pad_inv[P] |
+// pad_pair[P + E*127] | touched[E+1]
+constexpr size_t kNoAllocInts = (size_t)kNoAllocMaxE + (kNoAllocMaxE + 1) + 3 * (size_t)kNoAllocMaxPairs +
+                                ((size_t)kNoAllocMaxPairs + (size_t)kNoAllocMaxE * (kPadRows - 1)) +
+                                (kNoAllocMaxE + 1);
+
+__device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocInts];
+
+}  // namespace
+}  // namespace ds4moe
+
+extern "C" int ds4moe_route_noalloc(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_idx,
+                                    float* topk_w, int32_t* offsets, int32_t* perm_tok, ds4moe_stream_t stream) {
+  using namespace ds4moe;
+  auto misaligned = [](const void* p) { return ((uintptr_t)p & 15u) != 0; };
+  if (T < 0 || E < 1 || E > kNoAllocMaxE || k < 1 || k > 8 || k > E) return DS4MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * k > kNoAllocMaxPairs) return DS4MOE_ERR_TOO_MANY_TOKENS;
+  if (T == 0) return DS4MOE_OK;
+  if (!logits || !topk_idx || !topk_w || !offsets || !perm_tok) return DS4MOE_ERR_INVALID_ARG;
+  if (misaligned(logits) || misaligned(topk_idx) || misaligned(topk_w) || misaligned(offsets) || misaligned(perm_tok))
+    return DS4MOE_ERR_INVALID_ARG;
+
+  // Host code must not take the array's address directly (that is a host-side
+  // stand-in); the device address is looked up once per device, with that
+  // device current, on the first call made on it.
+  static std::mutex mu;
+  static int32_t* scratch_of[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!scratch_of[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return DS4MOE_ERR_CUDA;
+      }
+      scratch_of[dev] = static_cast<int32_t*>(p);
+    }
+    scratch = scratch_of[dev];
+  }
+  int32_t* counts = scratch;
+  int32_t* pad_offsets = counts + kNoAllocMaxE;
+  int32_t* perm_slot = pad_offsets + (kNoAllocMaxE + 1);
+  int32_t* inv = perm_slot + kNoAllocMaxPairs;
+  int32_t* pad_inv = inv + kNoAllocMaxPairs;
+  int32_t* pad_pair = pad_inv + kNoAllocMaxPairs;
+  int32_t* touched = pad_pair + (kNoAllocMaxPairs + kNoAllocMaxE * (kPadRows - 1));
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int blocks = (T + 7) / 8;
+  route_topk_kernel<<<blocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, nullptr, 0, nullptr, nullptr);
+  route_group_kernel<<<E, 256, 0, st>>>(topk_idx, T, E, k, counts, offsets, pad_offsets, perm_tok, perm_slot, inv,
+                                        pad_inv, pad_pair, touched);
+  if (cudaGetLastError() != cudaSuccess) return DS4MOE_ERR_CUDA;
+  return DS4MOE_OK;
+}
