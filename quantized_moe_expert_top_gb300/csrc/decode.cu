@@ -68,9 +68,12 @@ struct Ring {
 // Producer: stage s of this CTA holds rows [r0 + s*rps, r0 + (s+1)*rps) of the
 // global row list (clipped to r1); row r lives at base + grow(r) * pitch where
 // consecutive rows of one expert are consecutive in memory.
+// With `twin` set every row has a twin `twin_off` bytes further in global
+// memory (the up row of a gate row); twins land rps rows after the rows in the
+// stage.
 template <typename RowAddr>
-__device__ void produce(const Ring& R, int r0, int r1, int rps, int pitch, RowAddr row_addr, uint64_t budget,
-                        DeviceStatus* status, volatile int* abort_flag) {
+__device__ void produce(const Ring& R, int r0, int r1, int rps, int pitch, RowAddr row_addr, bool twin,
+                        size_t twin_off, uint64_t budget, DeviceStatus* status, volatile int* abort_flag) {
   const int nst = (r1 - r0 + rps - 1) / rps;
   uint32_t issued = 0, parity = 0;
   for (int s = 0; s < nst; ++s) {
@@ -82,14 +85,17 @@ __device__ void produce(const Ring& R, int r0, int r1, int rps, int pitch, RowAd
       break;
     }
     const int a = r0 + s * rps, b = min(a + rps, r1);
-    mbar_arrive_expect_tx(&R.full[slot], (uint32_t)((b - a) * pitch));
+    mbar_arrive_expect_tx(&R.full[slot], (uint32_t)((b - a) * pitch * (twin ? 2 : 1)));
     uint8_t* dst = R.buf + slot * R.stage_bytes;
     int seg = a;
-    while (seg < b) {  // contiguous segments (an expert boundary breaks a stage)
+    while (seg < b) {  // contiguous segments (a block or expert boundary breaks a stage)
       const uint8_t* src = row_addr(seg);
       int end = seg + 1;
       while (end < b && row_addr(end) == src + (size_t)(end - seg) * pitch) ++end;
       bulk_load(dst + (size_t)(seg - a) * pitch, src, (uint32_t)((end - seg) * pitch), &R.full[slot]);
+      if (twin)
+        bulk_load(dst + (size_t)(rps + seg - a) * pitch, src + twin_off, (uint32_t)((end - seg) * pitch),
+                  &R.full[slot]);
       seg = end;
     }
     issued |= 1u << slot;
@@ -149,8 +155,10 @@ __device__ Ring setup_ring(uint8_t* smem_raw, int stage_bytes) {
 }
 
 // ------------------------------------------------------------------ gate/up
-// Rows = every (gate row i, up row i) pair of every touched expert (one
-// interleaved gu row each); stage = kConsumers rows, one per consumer warp.
+// Rows = every (gate row i, up row i) pair of every touched expert; stage =
+// kConsumers gate rows then their kConsumers up rows, one pair per consumer
+// warp.  In the tile-major weight layout gate row i of expert e is row
+// (e*f/128 + i/128)*256 + i%128, its up row 128 rows later.
 __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
     const uint8_t* __restrict__ gu, int pitch, const uint4* __restrict__ xh, const float* __restrict__ xsig,
     float* __restrict__ out, int T, int d, int f, const int32_t* __restrict__ touched,
@@ -166,15 +174,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
       o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  const Ring R = setup_ring(smem_raw, kConsumers * pitch);
+  const Ring R = setup_ring(smem_raw, 2 * kConsumers * pitch);
   int r0, r1;
   cta_range(touched[E] * f, r0, r1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     if (lane == 0)
-      produce(R, r0, r1, kConsumers, pitch,
-              [&](int r) { return gu + ((size_t)__ldg(touched + r / f) * f + r % f) * pitch; }, budget, status,
-              abort_flag);
+      produce(
+          R, r0, r1, kConsumers, pitch,
+          [&](int r) {
+            const int i = r % f;
+            return gu + (((size_t)__ldg(touched + r / f) * (f / 128) + i / 128) * 256 + i % 128) * pitch;
+          },
+          true, (size_t)128 * pitch, budget, status, abort_flag);
     return;
   }
   const int cw = warp - 1;
@@ -185,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
     const int rp = r0 + s * kConsumers + cw;
     if (rp < r1) {
       const uint8_t* row = R.buf + (s % R.stages) * R.stage_bytes + cw * pitch;
+      const uint8_t* urow = row + kConsumers * pitch;
       const int e = __ldg(touched + rp / f), i = rp % f;
       const int p0 = __ldg(offsets + e), ne = __ldg(offsets + e + 1) - p0;
       for (int tg = 0; tg < ne; tg += kNT) {
@@ -198,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
           ag[tt] = au[tt] = 0.f;
         }
         for (int c = lane; c < nblk; c += 32) {
-          const uint4 gq = lds128(row + 16 * c), uq = lds128(row + d / 2 + 16 * c);
-          const float sg = e8m0_to_f32(row[d + c]), su = e8m0_to_f32(row[d + d / 32 + c]);
+          const uint4 gq = lds128(row + 16 * c), uq = lds128(urow + 16 * c);
+          const float sg = e8m0_to_f32(row[d / 2 + c]), su = e8m0_to_f32(urow[d / 2 + c]);
           uint32_t wg[16], wu[16];
           const uint32_t g4[4] = {gq.x, gq.y, gq.z, gq.w}, u4[4] = {uq.x, uq.y, uq.z, uq.w};
 #pragma unroll
@@ -264,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(
   if (warp == 0) {
     if (lane == 0)
       produce(R, r0, r1, rps, pitch, [&](int r) { return dn + ((size_t)__ldg(touched + r / d) * d + r % d) * pitch; },
-              budget, status, abort_flag);
+              false, 0, budget, status, abort_flag);
     return;
   }
   const int cw = warp - 1;
@@ -341,7 +354,7 @@ size_t ring_smem(int stage_bytes) {
 cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st) {
   (void)x;
   const int d = L->cfg.d_model, f = L->cfg.d_ff, E = L->cfg.n_experts;
-  const size_t smem = ring_smem(kConsumers * L->w.pitch_gu);
+  const size_t smem = ring_smem(2 * kConsumers * L->w.pitch_gu);
   cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   decode_gateup_kernel<<<L->num_sms, kThreads, smem, st>>>(

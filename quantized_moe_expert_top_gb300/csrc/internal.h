@@ -38,9 +38,9 @@ struct Scratch {
   float* xsig;           // [Tdec] the prescale 2^s of each row of xh
   float* h_dec;          // [Tdec*k][f] decode-path SwiGLU output (fp32, piece-transposed rows)
   uint8_t* xq;           // [pad_rows_max][d]   MXFP8 codes of x, padded expert order
-  uint8_t* xsf;          // [pad_rows_max/128][d/128][512] E8M0 scales (tcgen05 chunk layout)
+  uint8_t* xsf;          // [d/128][pad_rows_max/128][512] E8M0 scales (tcgen05 chunk layout)
   uint8_t* hq;           // [pad_rows_max][f]   MXFP8 codes of h (MXFP4 down)
-  uint8_t* hsf;          // [pad_rows_max/128][f/128][512]
+  uint8_t* hsf;          // [f/128][pad_rows_max/128][512]
   __half* h16;           // [pad_rows_max][f]   fp16 h (Q2_K down)
   uint8_t* stage_x;      // host-call staging: x [Tmax][d] bf16
   float* stage_logits;   // [Tmax][E]
@@ -49,16 +49,16 @@ struct Scratch {
 };
 
 // Weights as the kernels read them (library-owned device copies).
-//   gu: one row per (expert, i): gate codes (d/2 B) | up codes (d/2 B) |
-//       gate scales (d/32 B) | up scales (d/32 B) | padding to pitch_gu
-//       (a multiple of 32 B).  The decode path streams whole rows; the
-//       prefill TMA maps view the gate and up code columns with this pitch.
+//   gu: per (expert, 128-row block mb): the block's 128 gate rows, then its
+//       128 up rows; each row = codes (d/2 B) | E8M0 scales (d/32 B) |
+//       padding to pitch_gu (a multiple of 32 B).  The decode path streams
+//       rows; one prefill TMA box of 256 rows loads a gate tile and its up tile.
 //   dn: one row per (expert, m): codes (f/2 B) | scales (f/32 B) | padding.
 struct Weights {
-  uint8_t* gu;                       // [E][f][pitch_gu]
+  uint8_t* gu;                       // [E][f/128][2][128][pitch_gu]
   uint8_t* dn;                       // [E][d][pitch_dn] (MXFP4 down)
   int pitch_gu, pitch_dn;
-  uint8_t *gate_sf, *up_sf;          // [E][f/128][d/128][512] chunk layout (prefill)
+  uint8_t* gu_sf;                    // [E][f/128][d/128][gate 512 B | up 512 B] (prefill)
   uint8_t* down_sf;                  // [E][d/128][f/128][512]
   // Q2_K down, tile-major: one 3072-byte chunk per (expert, 128-row block,
   // 64-weight K step): 128 x 16 B 2-bit codes | 128 x 4 sub-block scale bytes
@@ -76,12 +76,11 @@ struct ds4moe_layer {
   ds4moe::Scratch s;
   ds4moe::DeviceStatus* status;  // device
   // TMA descriptors (64-byte aligned inside the struct)
-  CUtensorMap tm_gate;  // 4-bit weights, box 128 x 128
-  CUtensorMap tm_up;
-  CUtensorMap tm_down;
-  CUtensorMap tm_xq;    // 8-bit activations, box 128 x 32
-  CUtensorMap tm_hq;
-  CUtensorMap tm_h16;   // fp16 h, box 64 x 32
+  CUtensorMap tm_gu;     // 4-bit gate+up weights, box 128 x 256 rows
+  CUtensorMap tm_down;   // 4-bit down weights, box 128 x 128 rows
+  CUtensorMap tm_xq[3];  // 8-bit x, boxes 128 B x {32, 64, 128} rows
+  CUtensorMap tm_hq[3];  // 8-bit h
+  CUtensorMap tm_h16[3]; // fp16 h, boxes 64 x {32, 64, 128} rows
   cudaEvent_t ev[8];   // kernel timing events (created when timing is enabled)
   bool timing;
   int last_nk;         // kernels in the most recent forward
@@ -110,7 +109,9 @@ cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStrea
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
 
 // create-time repacking
-cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, cudaStream_t st);
+cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int chunk_stride,
+                             int chunk_off, cudaStream_t st);
+cudaError_t launch_pack_gu(const ds4moe_weights* w, ds4moe_layer* L, cudaStream_t st);
 cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream_t st);
 cudaError_t launch_pack_rows(uint8_t* dst, int pitch, int64_t rows, const uint8_t* s0, int l0, const uint8_t* s1,
                              int l1, const uint8_t* s2, int l2, const uint8_t* s3, int l3, cudaStream_t st);

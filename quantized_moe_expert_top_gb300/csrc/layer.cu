@@ -18,7 +18,10 @@ namespace {
 // tensor-core scale copy reads: per (expert, 128-row block, 128-K block) one
 // 512-byte chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kblock % 4) for row r of
 // the block.
-__global__ void repack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int rows, int K) {
+// (Chunk c of the output starts at c * chunk_stride + chunk_off bytes, so two
+// matrices' chunks can be interleaved.)
+__global__ void repack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int rows, int K,
+                                 int chunk_stride, int chunk_off) {
   const int nkb = K / 32;
   const size_t total = (size_t)E * rows * nkb;
   const int MB = rows / kBM, KB = K / kBK;
@@ -29,7 +32,27 @@ __global__ void repack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __res
     const int e = (int)(er / rows);
     const size_t chunk = ((size_t)e * MB + r / kBM) * KB + kb / 4;
     const int rr = r % kBM;
-    dst[chunk * kSfChunk + (rr % 32) * 16 + (rr / 32) * 4 + (kb % 4)] = src[i];
+    dst[chunk * chunk_stride + chunk_off + (rr % 32) * 16 + (rr / 32) * 4 + (kb % 4)] = src[i];
+  }
+}
+
+// Gate/up rows into the tile-major layout: for expert e and 128-row block mb,
+// 128 gate rows then the same 128 up rows, each codes | scales | padding.
+__global__ void pack_gu_kernel(uint8_t* __restrict__ dst, int pitch, int E, int d, int f,
+                               const uint8_t* __restrict__ gc, const uint8_t* __restrict__ gs,
+                               const uint8_t* __restrict__ uc, const uint8_t* __restrict__ us) {
+  const int64_t rows = (int64_t)E * f * 2;
+  for (int64_t R = blockIdx.x; R < rows; R += gridDim.x) {
+    const int r = (int)(R % 128);
+    const int j = (int)((R / 128) % 2);
+    const int64_t eb = R / 256;  // e * (f/128) + mb
+    const int64_t src_row = eb * 128 + r;  // = e * f + mb * 128 + r
+    const uint32_t* c = reinterpret_cast<const uint32_t*>((j ? uc : gc) + src_row * (d / 2));
+    const uint32_t* sc = reinterpret_cast<const uint32_t*>((j ? us : gs) + src_row * (d / 32));
+    uint32_t* o = reinterpret_cast<uint32_t*>(dst + R * pitch);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) o[i] = c[i];
+    for (int i = threadIdx.x; i < d / 128; i += blockDim.x) o[d / 8 + i] = sc[i];
+    for (int i = d / 8 + d / 128 + threadIdx.x; i < pitch / 4; i += blockDim.x) o[i] = 0u;
   }
 }
 
@@ -181,7 +204,9 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   if (!wts || !wts->gate_codes || !wts->gate_scales || !wts->up_codes || !wts->up_scales || !wts->down_codes)
     return DS4MOE_ERR_INVALID_ARG;
   if (cfg->down_format == DS4MOE_DOWN_MXFP4 && !wts->down_scales) return DS4MOE_ERR_INVALID_ARG;
-  if (!aligned16(wts->gate_codes) || !aligned16(wts->up_codes) || !aligned16(wts->down_codes))
+  if (!aligned16(wts->gate_codes) || !aligned16(wts->up_codes) || !aligned16(wts->down_codes) ||
+      !aligned16(wts->gate_scales) || !aligned16(wts->up_scales) ||
+      (wts->down_scales && !aligned16(wts->down_scales)))
     return DS4MOE_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -214,7 +239,7 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   const int Tdec = (cfg->force_path == DS4MOE_PATH_DECODE || Tm < cfg->decode_max_tokens) ? Tm
                                                                                           : cfg->decode_max_tokens;
   L->s.pad_rows_max = pad_rows;
-  L->w.pitch_gu = (d + d / 16 + 31) / 32 * 32;
+  L->w.pitch_gu = (d / 2 + d / 32 + 31) / 32 * 32;
   L->w.pitch_dn = (f / 2 + f / 32 + 31) / 32 * 32;
 
 #define TRY(x)                 \
@@ -225,11 +250,8 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   {
     Weights& w = L->w;
     Scratch& s = L->s;
-    TRY(alloc(L, &w.gu, (size_t)E * f * w.pitch_gu));
-    if (need_pre) {
-      TRY(alloc(L, &w.gate_sf, gu_scales));
-      TRY(alloc(L, &w.up_sf, gu_scales));
-    }
+    TRY(alloc(L, &w.gu, (size_t)E * f * 2 * w.pitch_gu));
+    if (need_pre) TRY(alloc(L, &w.gu_sf, 2 * gu_scales));
     if (!q2k) {
       TRY(alloc(L, &w.dn, (size_t)E * d * w.pitch_dn));
       if (need_pre) TRY(alloc(L, &w.down_sf, dn_scales));
@@ -287,17 +309,16 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
     }
     (void)gu_codes;
     (void)dn_codes;
-    if (launch_pack_rows(w.gu, w.pitch_gu, (int64_t)E * f, wts->gate_codes, d / 2, wts->up_codes, d / 2,
-                         wts->gate_scales, d / 32, wts->up_scales, d / 32, st) != cudaSuccess ||
+    if (launch_pack_gu(wts, L, st) != cudaSuccess ||
         (!q2k && launch_pack_rows(w.dn, w.pitch_dn, (int64_t)E * d, wts->down_codes, f / 2, wts->down_scales,
                                   f / 32, nullptr, 0, nullptr, 0, st) != cudaSuccess)) {
       rc = DS4MOE_ERR_CUDA;
       goto fail;
     }
     if (need_pre) {
-      if (launch_repack_sf(wts->gate_scales, w.gate_sf, E, f, d, st) != cudaSuccess ||
-          launch_repack_sf(wts->up_scales, w.up_sf, E, f, d, st) != cudaSuccess ||
-          (!q2k && launch_repack_sf(wts->down_scales, w.down_sf, E, d, f, st) != cudaSuccess)) {
+      if (launch_repack_sf(wts->gate_scales, w.gu_sf, E, f, d, 2 * kSfChunk, 0, st) != cudaSuccess ||
+          launch_repack_sf(wts->up_scales, w.gu_sf, E, f, d, 2 * kSfChunk, kSfChunk, st) != cudaSuccess ||
+          (!q2k && launch_repack_sf(wts->down_scales, w.down_sf, E, d, f, kSfChunk, 0, st) != cudaSuccess)) {
         rc = DS4MOE_ERR_CUDA;
         goto fail;
       }
@@ -307,20 +328,20 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       goto fail;
     }
     if (need_pre) {
-      bool tm_ok = encode_2d(&L->tm_gate, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu, d, (uint64_t)E * f,
-                             w.pitch_gu, 128, 128) &&
-                   encode_2d(&L->tm_up, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu + d / 2, d, (uint64_t)E * f,
-                             w.pitch_gu, 128, 128) &&
-                   encode_2d(&L->tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, 32);
-      if (!q2k) {
-        tm_ok = tm_ok &&
-                encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn, f, (uint64_t)E * d,
-                          w.pitch_dn, 128, 128) &&
-                encode_2d(&L->tm_hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, 32);
-      } else {
-        tm_ok = tm_ok && encode_2d(&L->tm_h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.h16, f, pad_rows, (uint64_t)f * 2,
-                                   64, 32);
+      bool tm_ok = encode_2d(&L->tm_gu, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu, d, (uint64_t)E * f * 2,
+                             w.pitch_gu, 128, 256);
+      static const uint32_t kBoxRows[3] = {32, 64, 128};
+      for (int b = 0; b < 3; ++b) {
+        tm_ok = tm_ok && encode_2d(&L->tm_xq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, kBoxRows[b]);
+        if (!q2k)
+          tm_ok = tm_ok && encode_2d(&L->tm_hq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, kBoxRows[b]);
+        else
+          tm_ok = tm_ok && encode_2d(&L->tm_h16[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.h16, f, pad_rows,
+                                     (uint64_t)f * 2, 64, kBoxRows[b]);
       }
+      if (!q2k)
+        tm_ok = tm_ok && encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn, f, (uint64_t)E * d,
+                                   w.pitch_dn, 128, 128);
       if (!tm_ok) {
         rc = DS4MOE_ERR_CUDA;
         goto fail;
@@ -511,10 +532,19 @@ void ds4moe_destroy(ds4moe_layer* L) {
 
 namespace ds4moe {
 
-cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, cudaStream_t st) {
+cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int chunk_stride,
+                             int chunk_off, cudaStream_t st) {
   const size_t total = (size_t)E * rows * (K / 32);
   const int blocks = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
-  repack_sf_kernel<<<blocks, 256, 0, st>>>(scales, sf, E, rows, K);
+  repack_sf_kernel<<<blocks, 256, 0, st>>>(scales, sf, E, rows, K, chunk_stride, chunk_off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_gu(const ds4moe_weights* w, ds4moe_layer* L, cudaStream_t st) {
+  const int64_t rows = (int64_t)L->cfg.n_experts * L->cfg.d_ff * 2;
+  const int grid = (int)(rows < 65536 ? rows : 65536);
+  pack_gu_kernel<<<grid, 128, 0, st>>>(L->w.gu, L->w.pitch_gu, L->cfg.n_experts, L->cfg.d_model, L->cfg.d_ff,
+                                       w->gate_codes, w->gate_scales, w->up_codes, w->up_scales);
   return cudaGetLastError();
 }
 

@@ -32,9 +32,15 @@ namespace {
 // each) to E4M3 with one E8M0 scale (s = floor(log2 amax) - 8, clamped; 0 for
 // an all-zero block), then writes the codes and the scale to the k padded rows
 // of the token's routed pairs.  Also zeroes out[t] for the down epilogue.
+// Activation scales use the K-block-major chunk layout [K/128][rows/128][512]
+// so the chunks of consecutive 128-row blocks are adjacent.
+__device__ __forceinline__ size_t act_sf_index(size_t row, int kblk, int r128) {
+  return ((size_t)(kblk / 4) * r128 + row / 128) * kSfChunk + (row % 32) * 16 + ((row % 128) / 32) * 4 + (kblk % 4);
+}
+
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k,
                                                         const int32_t* __restrict__ pad_inv, uint8_t* __restrict__ xq,
-                                                        uint8_t* __restrict__ xsf, float* __restrict__ out) {
+                                                        uint8_t* __restrict__ xsf, int r128, float* __restrict__ out) {
   const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -45,7 +51,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   int rows[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(pad_inv + (size_t)t * k + j) : 0;
-  const int nblk = d / 32, kgs = d / 128;
+  const int nblk = d / 32;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
   for (int c = lane; c < nblk; c += 32) {
     float v[32];
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
         uint4* dst = reinterpret_cast<uint4*>(xq + r * d + 32 * (size_t)c);
         dst[0] = c0;
         dst[1] = c1;
-        xsf[((r / 128) * kgs + c / 4) * kSfChunk + (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4)] = sb;
+        xsf[act_sf_index(r, c, r128)] = sb;
       }
     }
   }
@@ -119,6 +125,7 @@ struct Cfg<Mode::GateUp> {
   static constexpr int kSfSlot = 16;    // SFA gate 4 + SFA up 4 + SFB 8 columns
   static constexpr int kKs = 128;       // E2M1 / E4M3 elements per stage
   static constexpr int kDeqWarps = 0;
+  static constexpr int kEpiWarps = 12;  // three per tensor-memory lane quarter (SwiGLU + MXFP8 epilogue)
 };
 template <>
 struct Cfg<Mode::Down> {
@@ -129,6 +136,7 @@ struct Cfg<Mode::Down> {
   static constexpr int kSfSlot = 12;    // SFA 4 + SFB 8 columns
   static constexpr int kKs = 128;
   static constexpr int kDeqWarps = 0;
+  static constexpr int kEpiWarps = 8;   // two per lane quarter
 };
 template <>
 struct Cfg<Mode::DownQ2K> {
@@ -139,13 +147,13 @@ struct Cfg<Mode::DownQ2K> {
   static constexpr int kSfSlot = 0;
   static constexpr int kKs = 64;        // fp16 elements per stage
   static constexpr int kDeqWarps = 4;   // Q2_K -> fp16 producers, one weight row per thread
+  static constexpr int kEpiWarps = 8;
 };
 constexpr int kAccCol2 = 256;
 constexpr int kSfBase = 448;
 constexpr int kSfSlots = 4;
-constexpr int kEpiWarps = 8;           // two per tensor-memory lane quarter
 template <Mode M>
-constexpr int threads_of() { return 64 + 32 * kEpiWarps + 32 * Cfg<M>::kDeqWarps; }
+constexpr int threads_of() { return 64 + 32 * Cfg<M>::kEpiWarps + 32 * Cfg<M>::kDeqWarps; }
 constexpr int kPrefetchStages = 8;     // weight tiles prefetched into L2 ahead of their load
 static_assert(kSfSlots >= Cfg<Mode::GateUp>::kStages && kSfSlots >= Cfg<Mode::Down>::kStages, "scale slots");
 static_assert(kSfBase + kSfSlots * Cfg<Mode::GateUp>::kSfSlot <= 512, "tmem");
@@ -169,9 +177,9 @@ static_assert(Smem<Mode::DownQ2K>::kStage % 1024 == 0, "stage alignment");
 
 struct GemmArgs {
   // weights
-  const uint8_t* sfa0;  // chunk-layout scales of A0 (gate or down)
-  const uint8_t* sfa1;  // up
+  const uint8_t* sfa;   // chunk-layout scales of the A tile(s): kNumA x 512 B per (tile, K step)
   int rows_per_expert;  // f (gate/up) or d (down)
+  int r128;             // 128-row blocks of the activation buffers (scale layout pitch)
   int K;                // d (gate/up) or f (down)
   // activations (B)
   const uint8_t* sfb;   // chunk-layout scales of the B rows
@@ -246,10 +254,9 @@ struct StageIter {
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 template <Mode M>
-__global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
-                                                                       const __grid_constant__ CUtensorMap tm_a1,
-                                                                       const __grid_constant__ CUtensorMap tm_b,
-                                                                       const GemmArgs args) {
+__global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b32,
+    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b128, const GemmArgs args) {
   using C = Cfg<M>;
   using S = Smem<M>;
   extern __shared__ uint8_t smem_raw[];
@@ -279,14 +286,15 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
+      mbar_init(&acc_empty[b], C::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&tm_a0);
-    if (C::kNumA > 1) prefetch_tmap(&tm_a1);
-    prefetch_tmap(&tm_b);
+    if (M != Mode::DownQ2K) prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b32);
+    prefetch_tmap(&tm_b64);
+    prefetch_tmap(&tm_b128);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -309,11 +317,8 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
         if constexpr (M == Mode::DownQ2K) {
           bulk_prefetch_l2(args.q2k + tile * kQ2kChunk, kQ2kChunk);
         } else {
-          const int arow = p.it.e * args.rows_per_expert + p.it.mb * kBM;
-          tma_prefetch_2d(&tm_a0, p.kb * C::kKs, arow);
-          if (C::kNumA > 1) tma_prefetch_2d(&tm_a1, p.kb * C::kKs, arow);
-          bulk_prefetch_l2(args.sfa0 + tile * kSfChunk, kSfChunk);
-          if (C::kNumA > 1) bulk_prefetch_l2(args.sfa1 + tile * kSfChunk, kSfChunk);
+          tma_prefetch_2d(&tm_a, p.kb * C::kKs, (p.it.e * mb_per_e + p.it.mb) * kBM * C::kNumA);
+          bulk_prefetch_l2(args.sfa + tile * (C::kNumA * kSfChunk), C::kNumA * kSfChunk);
         }
       };
       for (int i = 0; i < kPrefetchStages && pf.valid; ++i) {
@@ -324,55 +329,70 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool fault_pending = args.debug_fault && blockIdx.x == 0;
-      while (ld.valid) {
-        const int N = round16(ld.it.nch);
-        const int nb = (N + 31) / 32, nsf = (N + 127) / 128;
-        const int prow = __ldg(args.pad_offsets + ld.it.e) + ld.it.t0;
-        const int arow = ld.it.e * args.rows_per_expert + ld.it.mb * kBM;
+      bool ok = true;
+      UnitIter it = ld.it;
+      for (bool more = ld.valid; more && ok; more = it.next()) {
+        // per-chunk constants
+        const int N = round16(it.nch);
+        const int nsf = (N + 127) / 128;
+        // token rows in TMA boxes of 128 / 64 / 32 rows (at most two for N <= 192)
+        uint32_t boxes = 0;  // 2 bits per box: 0 = 32 rows, 1 = 64, 2 = 128
+        int nbox = 0, brows = 0;
+        {
+          int rem = N;
+          while (rem >= 128) { boxes |= 2u << (2 * nbox++); rem -= 128; brows += 128; }
+          if (rem > 64) { boxes |= 2u << (2 * nbox++); brows += 128; }
+          else if (rem > 32) { boxes |= 1u << (2 * nbox++); brows += 64; }
+          else if (rem > 0) { nbox++; brows += 32; }
+        }
+        const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+        const int arow = (it.e * mb_per_e + it.mb) * kBM * C::kNumA;  // gate+up: 256-row box
         // A 4-bit unpacking load counts its packed global bytes (half the
         // 16 KB it writes to shared memory).
         const uint32_t bytes = M == Mode::DownQ2K
-                                   ? (uint32_t)(nb * 32 * 128 + kQ2kChunk)
-                                   : (uint32_t)(C::kNumA * S::kA / 2 + nb * 32 * 128 + (C::kNumA + nsf) * kSfChunk);
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
-          report_timeout(args.status, kWhereProducerEmpty);
-          *abort_flag = 1;
-          break;
-        }
-        uint8_t* st = smem + stage * S::kStage;
-        uint8_t* sa0 = st;
-        uint8_t* sa1 = st + S::kA;
-        uint8_t* sb = st + C::kNumA * S::kA;
-        uint8_t* ssf = sb + S::kB;
-        (void)sa1;
-        const int kb = ld.kb;
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        const size_t tile = ((size_t)(ld.it.e * mb_per_e + ld.it.mb) * KB + kb);
-        if (fault_pending) {
-          fault_pending = false;  // test-only: drop this stage's loads
-        } else if constexpr (M == Mode::DownQ2K) {
-          for (int i = 0; i < nb; ++i) tma_load_2d(sb + i * 32 * 128, &tm_b, &full[stage], kb * C::kKs, prow + 32 * i);
-          bulk_load(ssf, args.q2k + tile * kQ2kChunk, kQ2kChunk, &full[stage]);
-        } else {
-          tma_load_2d(sa0, &tm_a0, &full[stage], kb * C::kKs, arow);
-          if (C::kNumA > 1) tma_load_2d(sa1, &tm_a1, &full[stage], kb * C::kKs, arow);
-          for (int i = 0; i < nb; ++i) tma_load_2d(sb + i * 32 * 128, &tm_b, &full[stage], kb * C::kKs, prow + 32 * i);
-          bulk_load(ssf, args.sfa0 + tile * kSfChunk, kSfChunk, &full[stage]);
-          if (C::kNumA > 1) bulk_load(ssf + kSfChunk, args.sfa1 + tile * kSfChunk, kSfChunk, &full[stage]);
-          for (int i = 0; i < nsf; ++i)
-            bulk_load(ssf + (C::kNumA + i) * kSfChunk, args.sfb + ((size_t)(prow / 128 + i) * KB + kb) * kSfChunk,
-                      kSfChunk, &full[stage]);
-        }
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        ld.next();
-        if (pf.valid) {
-          prefetch(pf);
-          pf.next();
+                                   ? (uint32_t)(brows * 128 + kQ2kChunk)
+                                   : (uint32_t)(C::kNumA * S::kA / 2 + brows * 128 + (C::kNumA + nsf) * kSfChunk);
+        const size_t tile0 = (size_t)(it.e * mb_per_e + it.mb) * KB;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
+            report_timeout(args.status, kWhereProducerEmpty);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * S::kStage;
+          uint8_t* sb = st + C::kNumA * S::kA;
+          uint8_t* ssf = sb + S::kB;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          if (fault_pending) {
+            fault_pending = false;  // test-only: drop this stage's loads
+          } else {
+            int r = 0;
+            for (int i = 0; i < nbox; ++i) {
+              const uint32_t bx = (boxes >> (2 * i)) & 3u;
+              const CUtensorMap* tb = bx == 2 ? &tm_b128 : (bx == 1 ? &tm_b64 : &tm_b32);
+              tma_load_2d(sb + r * 128, tb, &full[stage], kb * C::kKs, prow + r);
+              r += 32 << bx;
+            }
+            if constexpr (M == Mode::DownQ2K) {
+              bulk_load(ssf, args.q2k + (tile0 + kb) * kQ2kChunk, kQ2kChunk, &full[stage]);
+            } else {
+              tma_load_2d(st, &tm_a, &full[stage], kb * C::kKs, arow);
+              bulk_load(ssf, args.sfa + (tile0 + kb) * (C::kNumA * kSfChunk), C::kNumA * kSfChunk, &full[stage]);
+              bulk_load(ssf + C::kNumA * kSfChunk, args.sfb + ((size_t)kb * args.r128 + prow / 128) * kSfChunk,
+                        nsf * kSfChunk, &full[stage]);
+            }
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (pf.valid) {
+            prefetch(pf);
+            pf.next();
+          }
         }
       }
       if (*abort_flag) {
@@ -394,11 +414,22 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
       uint32_t sf_seq = 0;  // running stage count; slot = sf_seq % kSfSlots (kSfSlots >= kStages)
       int chunk = 0;
       bool ok = true;
+      // Shared-memory descriptors of every stage slot, computed once: K steps
+      // add 32 bytes (2 in the 16-byte address field) to the start address.
+      // (Only the 14-bit start-address field differs between slots, so a slot
+      // is the slot-0 descriptor plus slot * stage size in 16-byte units.)
+      const uint32_t st0 = smem_u32(smem);
+      const uint64_t adesc0 = smem_desc(st0, 16, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(st0 + C::kNumA * S::kA, 16, 1024, 2);
+      const uint64_t sfdesc0 = smem_desc(st0 + C::kNumA * S::kA + S::kB, 0, 128, 0);
+      static_assert(C::kStages * S::kStage < (1 << 18), "descriptor address field");
       for (bool more = it.first_chunk(); more && ok; more = it.next(), ++chunk) {
         const int N = round16(it.nch);
         const int nsf = (N + 127) / 128;
         const int buf = chunk % C::kAccBufs;
         const uint32_t acc0 = tmem + (uint32_t)(buf * kAccCol2);
+        const uint32_t idesc0 = M == Mode::DownQ2K ? idesc_f16(N) : idesc_mx(N, 0);
+        constexpr uint32_t kSfIdStep = (1u << 4) | (1u << 29);  // next byte of the 32-bit scale word, A and B
         if (!mbar_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
           report_timeout(args.status, kWhereMmaAccEmpty);
           *abort_flag = 1;
@@ -422,31 +453,25 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
             }
           }
           tc_fence_after();
-          uint8_t* st = smem + stage * S::kStage;
-          const uint32_t a0 = smem_u32(st), a1 = smem_u32(st + S::kA);
-          const uint32_t b = smem_u32(st + C::kNumA * S::kA);
-          const uint32_t ssf = b + S::kB;
-          (void)a1;
+          const uint64_t soff = (uint64_t)(stage * (S::kStage >> 4));
+          const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
           if constexpr (M == Mode::DownQ2K) {
-            const uint32_t idesc = idesc_f16(N);
 #pragma unroll
             for (int j = 0; j < 4; ++j)  // K = 16 fp16 (32 bytes) per instruction
-              mma_f16(acc0, smem_desc(a0 + 32 * j, 16, 1024, 2), smem_desc(b + 32 * j, 16, 1024, 2), idesc,
-                      (kb > 0 || j > 0) ? 1u : 0u);
+              mma_f16(acc0, ad + 2 * j, bd + 2 * j, idesc0, (kb > 0 || j > 0) ? 1u : 0u);
           } else {
             const uint32_t slot = tmem + kSfBase + (sf_seq++ % kSfSlots) * C::kSfSlot;
-            // scale factors -> tensor memory: A chunk(s) at slot+0 (+4), B chunks after
-            for (int i = 0; i < C::kNumA + nsf; ++i)
-              tc_cp_32x128b_warpx4(slot + 4 * i, smem_desc(ssf + i * kSfChunk, 0, 128, 0));
+            // scale factors -> tensor memory: A chunk(s) at slot+0 (+4), B chunks after (512 B = 32 units)
+            const uint64_t sd = sfdesc0 + soff;
+            for (int i = 0; i < C::kNumA + nsf; ++i) tc_cp_32x128b_warpx4(slot + 4 * i, sd + 32 * i);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {  // K = 32 (32 bytes) per instruction
-              const uint32_t idesc = idesc_mx(N, (uint32_t)j);
-              const uint64_t bd = smem_desc(b + 32 * j, 16, 1024, 2);
+              const uint32_t idesc = idesc0 + (uint32_t)j * kSfIdStep;
               const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-              mma_mxf8f6f4(acc0, smem_desc(a0 + 32 * j, 16, 1024, 2), bd, idesc, slot, slot + 4 * C::kNumA, accum);
-              if (C::kNumA > 1)
-                mma_mxf8f6f4(acc0 + kAccCol2, smem_desc(a1 + 32 * j, 16, 1024, 2), bd, idesc, slot + 4,
-                             slot + 4 * C::kNumA, accum);
+              mma_mxf8f6f4(acc0, ad + 2 * j, bd + 2 * j, idesc, slot, slot + 4 * C::kNumA, accum);
+              if (C::kNumA > 1)  // up tile: 16 KB (1024 address units) after the gate tile
+                mma_mxf8f6f4(acc0 + kAccCol2, ad + 1024 + 2 * j, bd + 2 * j, idesc, slot + 4, slot + 4 * C::kNumA,
+                             accum);
             }
           }
           tc_commit(&empty[stage]);
@@ -464,10 +489,10 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
       mbar_wait_bounded(drain, 0, args.budget_ns, &never);
     }
     __syncwarp();
-  } else if (warp >= 2 + kEpiWarps) {
+  } else if (warp >= 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ Q2_K dequant
     if constexpr (M == Mode::DownQ2K) {
-      const int r = (warp - 2 - kEpiWarps) * 32 + lane;  // weight row of the 128-row tile
+      const int r = (warp - 2 - C::kEpiWarps) * 32 + lane;  // weight row of the 128-row tile
       StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax},
                    0, KB, false};
       sq.start();
@@ -528,8 +553,9 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // tensor-memory lane quarter this warp may access
-    const int half = (warp - 2) >> 2;   // which half of the 16-column chunks
-    const int etid = threadIdx.x - 64;  // 0..255 among the epilogue warps
+    const int part = (warp - 2) >> 2;   // which share of the 16-column chunks
+    constexpr int kParts = C::kEpiWarps / 4;
+    const int etid = threadIdx.x - 64;  // index among the epilogue threads
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
     uint32_t acc_phase = 0;
@@ -544,8 +570,8 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
         // thread takes the accumulator wait and publishes the outcome, so all
         // epilogue warps leave the loop together (the named barriers need
         // every one of them).
-        named_bar_sync(1, 32 * kEpiWarps);  // previous chunk's table no longer read
-        for (int c = etid; c < it.nch; c += 32 * kEpiWarps) {
+        named_bar_sync(1, 32 * C::kEpiWarps);  // previous chunk's table no longer read
+        for (int c = etid; c < it.nch; c += 32 * C::kEpiWarps) {
           const int pair = __ldg(args.pad_pair + prow + c);
           col_tok[c] = pair / args.k;
           col_w[c] = __ldg(args.topk_w + pair);
@@ -558,7 +584,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
             *abort_flag = 1;
           }
         }
-        named_bar_sync(1, 32 * kEpiWarps);
+        named_bar_sync(1, 32 * C::kEpiWarps);
         got = (uint32_t)*epi_ok;
         if (!got) break;
       } else {
@@ -577,7 +603,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
       tc_fence_after();
       const uint32_t acc0 = tmem + (uint32_t)(buf * kAccCol2) + lane_base;
       const int unit_row = it.mb * kBM + q * 32 + lane;  // row of this lane inside the expert
-      for (int c0 = half * 16; c0 < N; c0 += 32) {
+      for (int c0 = part * 16; c0 < N; c0 += 16 * kParts) {
         uint32_t r0[16];
         tmem_ld_32x32b_x16(acc0 + (uint32_t)c0, r0);
         if (M == Mode::GateUp) {
@@ -608,11 +634,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
                 if (a > 0.f) s = max(-127, min(127, floor_log2_f32(a) - 8));
                 const size_t row = (size_t)(prow + col);
                 args.hq[row * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
-                if (lane == 0) {
-                  const int kblk = i / 32;
-                  args.hsf[((row / 128) * (size_t)(args.f / 128) + kblk / 4) * kSfChunk + (row % 32) * 16 +
-                           ((row % 128) / 32) * 4 + (kblk % 4)] = (uint8_t)(s + 127);
-                }
+                if (lane == 0) args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
               }
             }
           }
@@ -642,15 +664,15 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
 }
 
 template <Mode M>
-cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a, const CUtensorMap* b, const GemmArgs& args,
+                        cudaStream_t st) {
   static_assert(Smem<M>::kTotal <= 227 * 1024, "shared memory");
   const void* fn = (const void*)grouped_gemm_kernel<M>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<M>::kTotal);
   if (e != cudaSuccess) return e;
   const int units = args.E * (args.rows_per_expert / kBM);
   const int grid = units < L->num_sms ? units : L->num_sms;
-  grouped_gemm_kernel<M><<<grid, threads_of<M>(), Smem<M>::kTotal, st>>>(a0, a1, b, args);
+  grouped_gemm_kernel<M><<<grid, threads_of<M>(), Smem<M>::kTotal, st>>>(a, b[0], b[1], b[2], args);
   return cudaGetLastError();
 }
 
@@ -659,7 +681,7 @@ cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a0, const CUte
 cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st) {
   const int blocks = (T + 7) / 8;
   act_quant_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T, L->cfg.d_model, L->cfg.top_k,
-                                           L->s.pad_inv, L->s.xq, L->s.xsf, out);
+                                           L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), out);
   return cudaGetLastError();
 }
 
@@ -674,6 +696,7 @@ static GemmArgs base_args(const ds4moe_layer* L) {
   a.d = L->cfg.d_model;
   a.f = L->cfg.d_ff;
   a.status = L->status;
+  a.r128 = (int)(L->s.pad_rows_max / 128);
   a.debug_fault = L->cfg.debug_fault;
   a.budget_ns = L->cfg.debug_fault ? 1000000ull : (uint64_t)L->cfg.wait_timeout_ms * 1000000ull;
   return a;
@@ -682,28 +705,26 @@ static GemmArgs base_args(const ds4moe_layer* L) {
 cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, cudaStream_t st) {
   (void)T;
   GemmArgs a = base_args(L);
-  a.sfa0 = L->w.gate_sf;
-  a.sfa1 = L->w.up_sf;
+  a.sfa = L->w.gu_sf;
   a.rows_per_expert = L->cfg.d_ff;
   a.K = L->cfg.d_model;
   a.sfb = L->s.xsf;
   a.hq = L->s.hq;
   a.hsf = L->s.hsf;
   a.h16 = (L->cfg.down_format == DS4MOE_DOWN_Q2K) ? L->s.h16 : nullptr;
-  return launch_gemm<Mode::GateUp>(L, L->tm_gate, L->tm_up, L->tm_xq, a, st);
+  return launch_gemm<Mode::GateUp>(L, L->tm_gu, L->tm_xq, a, st);
 }
 
 cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
   (void)T;
   GemmArgs a = base_args(L);
   a.debug_fault = 0;
-  a.sfa0 = L->w.down_sf;
-  a.sfa1 = L->w.down_sf;
+  a.sfa = L->w.down_sf;
   a.rows_per_expert = L->cfg.d_model;
   a.K = L->cfg.d_ff;
   a.sfb = L->s.hsf;
   a.out = out;
-  return launch_gemm<Mode::Down>(L, L->tm_down, L->tm_down, L->tm_hq, a, st);
+  return launch_gemm<Mode::Down>(L, L->tm_down, L->tm_hq, a, st);
 }
 
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
@@ -714,7 +735,7 @@ cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaS
   a.rows_per_expert = L->cfg.d_model;
   a.K = L->cfg.d_ff;
   a.out = out;
-  return launch_gemm<Mode::DownQ2K>(L, L->tm_h16, L->tm_h16, L->tm_h16, a, st);
+  return launch_gemm<Mode::DownQ2K>(L, L->tm_h16[0], L->tm_h16, a, st);
 }
 
 int prefill_launches() { return 5; }
