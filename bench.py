@@ -239,7 +239,9 @@ def measure_workload(ds4, layer, wl, steps, warmup, peaks, flush, want_kernels=T
            "TFLOPs": acc["flops"] / (ms * 1e-3) / 1e12,
            "hbm_frac_of_measured": acc["total_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
            "kernels_ms": {k: statistics.median(v) for k, v in kern.items()},
-           "launches": layer.launches_per_forward(wl.T)}
+           "launches": layer.launches_per_forward(wl.T),
+           "path": {1: "decode (CUDA-core GEMV)", 2: "prefill (MXFP8 tcgen05 GEMM)",
+                    3: "decode_mma (split-precision tcgen05 GEMM)"}.get(layer.path_for(wl.T), "?")}
     return res, acc, x, logits, out
 
 
@@ -326,6 +328,21 @@ def run_ours(args):
     # ---- the other workloads, same GPU (rank 0 reports them)
     also = {}
     if not args.no_extra:
+        gemv = None
+        if layer_wl.down != "q2k":  # the CUDA-core GEMV decode path, for comparison
+            Wg = synth.make_layer_weights(layer_wl, device="cuda")
+            gemv = ds4.Layer(layer_wl.d, layer_wl.E, layer_wl.f, layer_wl.k, 64, Wg, force_path="decode")
+            del Wg
+            torch.cuda.empty_cache()
+            for name in ("decode1", "decode64"):
+                other = synth.WORKLOADS[name]
+                try:
+                    r, a, *_ = measure_workload(ds4, gemv, other, min(args.steps, 20), args.warmup, peaks, L2Flush())
+                    also[name + "_gemv_path"] = dict(r, algorithmic_bytes=a["total_bytes"])
+                except Exception as exc:
+                    also[name + "_gemv_path"] = {"error": str(exc)}
+            gemv.close()
+            torch.cuda.empty_cache()
         for name in ("decode1", "decode64", "prefill", "q2k"):
             if name == wl.name:
                 continue

@@ -21,11 +21,16 @@
  *   5. down     y = W_down[e] h.
  *   6. combine  out[t] = sum_j w[t, j] * y[t, j]   (fp32).
  *
- * Two execution paths compute it (chosen per call, see ds4moe_path_for):
- *   DECODE  (T <= decode_max_tokens): weights streamed through registers,
- *           activations kept at bf16/fp32 precision.
- *   PREFILL (larger T): grouped block-scaled tcgen05 GEMMs; x and h are
- *           quantised to MXFP8 (E4M3 + one E8M0 scale per 32 values, OCP MX
+ * Three execution paths compute it (chosen per call, see ds4moe_path_for):
+ *   DECODE_MMA (AUTO for T <= decode_max_tokens): the grouped tcgen05 GEMMs
+ *           below with split-precision activations: every x (and h) row is
+ *           sent as two MXFP8 rows, hi = MXFP8(v) and lo = MXFP8(v - hi), and
+ *           the epilogues add the two products, so activations keep about
+ *           bf16 precision while the weights stay 4-bit.
+ *   DECODE  (only when forced): memory-streaming GEMVs on the CUDA cores,
+ *           weights dequantised in registers, activations at f16/fp32.
+ *   PREFILL (AUTO for larger T): grouped block-scaled tcgen05 GEMMs; x and h
+ *           are quantised to MXFP8 (E4M3 + one E8M0 scale per 32 values, OCP MX
  *           v1.0 conversion rule) inside the library; with a Q2_K down
  *           projection h is kept in fp16 instead.
  *
@@ -73,7 +78,7 @@ enum {
 };
 
 enum { DS4MOE_DOWN_MXFP4 = 0, DS4MOE_DOWN_Q2K = 1 };
-enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2 };
+enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2, DS4MOE_PATH_DECODE_MMA = 3 };
 
 /* Layer shape and options.  Fill with ds4moe_config_default() first.
  *   d_model    hidden size d; multiple of 128, 128..8192.
@@ -83,9 +88,9 @@ enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2 };
  *   top_k      experts per token k; 1..min(8, E).
  *   max_tokens largest T a forward call may pass (scratch is sized for it).
  *   down_format      DS4MOE_DOWN_MXFP4 or DS4MOE_DOWN_Q2K.  A Q2_K layer runs
- *                    every call on the PREFILL path (DECODE streams MXFP4 only;
- *                    force_path = DECODE is then UNSUPPORTED).
- *   decode_max_tokens  AUTO path choice: T <= this runs DECODE (default 64).
+ *                    every call on the PREFILL path (the decode paths stream
+ *                    MXFP4 only; forcing one of them is then UNSUPPORTED).
+ *   decode_max_tokens  AUTO path choice: T <= this runs DECODE_MMA (default 64).
  *   force_path       DS4MOE_PATH_* (AUTO by default; tests force a path).
  *   debug_fault      0 in production.  1 = the first prefill GEMM drops one
  *                    of its operand loads and its waits give up after ~1 ms,
@@ -163,8 +168,8 @@ int ds4moe_get_routing(ds4moe_layer *layer, int32_t *topk_idx, float *topk_w, in
  * DS4MOE_ERR_CUDA. */
 int ds4moe_get_status(ds4moe_layer *layer);
 
-/* DS4MOE_PATH_DECODE or DS4MOE_PATH_PREFILL for a call with T tokens, or a
- * negative error for a NULL layer / T out of range. */
+/* DS4MOE_PATH_DECODE, _PREFILL or _DECODE_MMA for a call with T tokens, or
+ * a negative error for a NULL layer / T out of range. */
 int ds4moe_path_for(const ds4moe_layer *layer, int32_t T);
 
 /* Number of kernels one ds4moe_forward(T) enqueues (0 for T = 0), or a
@@ -176,7 +181,8 @@ int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
  * after each kernel.  ds4moe_kernel_times() synchronises that stream and writes
  * the elapsed milliseconds of each kernel of the most recent forward, in
  * launch order (DECODE: route_topk, route_group, decode_gateup, decode_down;
- * PREFILL: route_topk, route_group, act_quant, gemm_gateup, gemm_down), and
+ * PREFILL and DECODE_MMA: route_topk, route_group, act_quant, gemm_gateup,
+ * gemm_down), and
  * returns how many it wrote (at most max_n), or a negative error.
  * ds4moe_kernel_name() gives those names (NULL past the end). */
 int ds4moe_set_kernel_timing(ds4moe_layer *layer, int enable);

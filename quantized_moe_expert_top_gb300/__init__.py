@@ -8,7 +8,7 @@ built in-tree by :func:`build`.
 from ._binding import (  # noqa: F401
     Config, Ds4moeError, Layer, WeightPtrs, default_config, header_functions, lib, route_noalloc, status_string,
     OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TOO_MANY_TOKENS, ERR_DEVICE_TIMEOUT,
-    DOWN_MXFP4, DOWN_Q2K, PATH_AUTO, PATH_DECODE, PATH_PREFILL, LIB_PATH,
+    DOWN_MXFP4, DOWN_Q2K, PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_DECODE_MMA, LIB_PATH,
 )
 
 

@@ -27,8 +27,8 @@ ERR_TOO_MANY_TOKENS = -5
 ERR_DEVICE_TIMEOUT = -6
 
 DOWN_MXFP4, DOWN_Q2K = 0, 1
-PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
-_PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "prefill": PATH_PREFILL}
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_DECODE_MMA = 0, 1, 2, 3
+_PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "prefill": PATH_PREFILL, "decode_mma": PATH_DECODE_MMA}
 _DOWN = {"mxfp4": DOWN_MXFP4, "q2k": DOWN_Q2K}
 
 

@@ -20,6 +20,7 @@ constexpr int kSfChunk = 512;     // bytes of one scale-factor chunk (128 rows x
 constexpr int kGateUpNMax = 224;  // token columns per gate/up tile (two accumulators in TMEM)
 constexpr int kDownNMax = 256;    // token columns per down tile
 constexpr int kQ2kChunk = 3072;   // bytes of one Q2_K tile-major chunk
+constexpr int kNumBoxMaps = 12;   // token-tile TMA maps with 16, 32, ..., 192-row boxes
 
 // Routing tables and scratch for one forward call (all device memory).
 struct Scratch {
@@ -78,9 +79,9 @@ struct ds4moe_layer {
   // TMA descriptors (64-byte aligned inside the struct)
   CUtensorMap tm_gu;     // 4-bit gate+up weights, box 128 x 256 rows
   CUtensorMap tm_down;   // 4-bit down weights, box 128 x 128 rows
-  CUtensorMap tm_xq[3];  // 8-bit x, boxes 128 B x {32, 64, 128} rows
-  CUtensorMap tm_hq[3];  // 8-bit h
-  CUtensorMap tm_h16[3]; // fp16 h, boxes 64 x {32, 64, 128} rows
+  CUtensorMap tm_xq[ds4moe::kNumBoxMaps];   // 8-bit x, boxes 128 B x (16 * (i + 1)) rows
+  CUtensorMap tm_hq[ds4moe::kNumBoxMaps];   // 8-bit h
+  CUtensorMap tm_h16[ds4moe::kNumBoxMaps];  // fp16 h, boxes 64 x (16 * (i + 1)) rows
   cudaEvent_t ev[8];   // kernel timing events (created when timing is enabled)
   bool timing;
   int last_nk;         // kernels in the most recent forward
@@ -98,14 +99,16 @@ namespace ds4moe {
 // Each returns cudaSuccess or the launch error; none synchronises.
 cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
                               cudaStream_t st);
-cudaError_t launch_route_group(const ds4moe_layer* L, int T, cudaStream_t st);
+cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream_t st);
 
 cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st);
 cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
 
-cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st);
-cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, cudaStream_t st);
-cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+// split = 2: every routed pair has two activation rows, hi = MXFP8(v) and
+// lo = MXFP8(v - hi); the GEMM epilogues add the two columns back together.
+cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, int split, cudaStream_t st);
+cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStream_t st);
+cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
 
 // create-time repacking

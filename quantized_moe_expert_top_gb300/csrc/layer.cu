@@ -140,7 +140,7 @@ int validate_config(const ds4moe_config* c) {
   if (c->down_format != DS4MOE_DOWN_MXFP4 && c->down_format != DS4MOE_DOWN_Q2K) return DS4MOE_ERR_INVALID_ARG;
   if (c->down_format == DS4MOE_DOWN_Q2K && c->d_ff % 256) return DS4MOE_ERR_UNSUPPORTED;
   if (c->decode_max_tokens < 0) return DS4MOE_ERR_INVALID_ARG;
-  if (c->force_path < DS4MOE_PATH_AUTO || c->force_path > DS4MOE_PATH_PREFILL) return DS4MOE_ERR_INVALID_ARG;
+  if (c->force_path < DS4MOE_PATH_AUTO || c->force_path > DS4MOE_PATH_DECODE_MMA) return DS4MOE_ERR_INVALID_ARG;
   if (c->wait_timeout_ms < 1 || c->wait_timeout_ms > 60000) return DS4MOE_ERR_INVALID_ARG;
   return DS4MOE_OK;
 }
@@ -161,10 +161,9 @@ int alloc(ds4moe_layer* L, Tp** p, size_t bytes) {
 }
 
 int path_of(const ds4moe_layer* L, int T) {
-  if (L->cfg.down_format == DS4MOE_DOWN_Q2K) return DS4MOE_PATH_PREFILL;  // decode path streams MXFP4 only
-  if (L->cfg.force_path == DS4MOE_PATH_DECODE) return DS4MOE_PATH_DECODE;
-  if (L->cfg.force_path == DS4MOE_PATH_PREFILL) return DS4MOE_PATH_PREFILL;
-  return T <= L->cfg.decode_max_tokens ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
+  if (L->cfg.down_format == DS4MOE_DOWN_Q2K) return DS4MOE_PATH_PREFILL;  // decode paths stream MXFP4 only
+  if (L->cfg.force_path != DS4MOE_PATH_AUTO) return L->cfg.force_path;
+  return T <= L->cfg.decode_max_tokens ? DS4MOE_PATH_DECODE_MMA : DS4MOE_PATH_PREFILL;
 }
 
 void free_all(ds4moe_layer* L) {
@@ -226,18 +225,22 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   const size_t gu_codes = (size_t)E * f * (d / 2), gu_scales = (size_t)E * f * (d / 32);
   const size_t dn_codes = (size_t)E * d * (f / 2), dn_scales = (size_t)E * d * (f / 32);
   const int64_t pairs = (int64_t)Tm * k;
-  const int64_t pad_rows = ((pairs + (int64_t)E * (kPadRows - 1)) + kPadRows - 1) / kPadRows * kPadRows;
   const bool q2k = cfg->down_format == DS4MOE_DOWN_Q2K;
-  if (q2k && cfg->force_path == DS4MOE_PATH_DECODE) {  // the decode path streams MXFP4 rows only
-    delete L;
+  if (q2k && (cfg->force_path == DS4MOE_PATH_DECODE || cfg->force_path == DS4MOE_PATH_DECODE_MMA)) {
+    delete L;  // the decode paths stream MXFP4 only
     return DS4MOE_ERR_UNSUPPORTED;
   }
-  const bool need_dec = !q2k && cfg->force_path != DS4MOE_PATH_PREFILL &&
-                        (cfg->force_path == DS4MOE_PATH_DECODE || cfg->decode_max_tokens > 0);
-  const bool need_pre = q2k || cfg->force_path == DS4MOE_PATH_PREFILL ||
-                        (cfg->force_path == DS4MOE_PATH_AUTO && Tm > cfg->decode_max_tokens);
-  const int Tdec = (cfg->force_path == DS4MOE_PATH_DECODE || Tm < cfg->decode_max_tokens) ? Tm
-                                                                                          : cfg->decode_max_tokens;
+  // GEMV buffers only when that path is forced; the GEMM buffers serve PREFILL and DECODE_MMA.
+  const bool need_dec = !q2k && cfg->force_path == DS4MOE_PATH_DECODE;
+  const bool need_pre = cfg->force_path != DS4MOE_PATH_DECODE;
+  const bool split_ok = !q2k && (cfg->force_path == DS4MOE_PATH_DECODE_MMA ||
+                                 (cfg->force_path == DS4MOE_PATH_AUTO && cfg->decode_max_tokens > 0));
+  const int Tdec = (cfg->force_path != DS4MOE_PATH_AUTO || Tm < cfg->decode_max_tokens) ? Tm
+                                                                                       : cfg->decode_max_tokens;
+  // padded activation rows: one per routed pair (PREFILL), two (DECODE_MMA)
+  const int64_t split_rows = split_ok ? 2 * (int64_t)Tdec * k : 0;
+  const int64_t rows_needed = (pairs > split_rows ? pairs : split_rows) + (int64_t)E * (kPadRows - 1);
+  const int64_t pad_rows = (rows_needed + kPadRows - 1) / kPadRows * kPadRows;
   L->s.pad_rows_max = pad_rows;
   L->w.pitch_gu = (d / 2 + d / 32 + 31) / 32 * 32;
   L->w.pitch_dn = (f / 2 + f / 32 + 31) / 32 * 32;
@@ -330,14 +333,14 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
     if (need_pre) {
       bool tm_ok = encode_2d(&L->tm_gu, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu, d, (uint64_t)E * f * 2,
                              w.pitch_gu, 128, 256);
-      static const uint32_t kBoxRows[3] = {32, 64, 128};
-      for (int b = 0; b < 3; ++b) {
-        tm_ok = tm_ok && encode_2d(&L->tm_xq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, kBoxRows[b]);
+      for (int b = 0; b < kNumBoxMaps; ++b) {
+        const uint32_t rows = 16u * (uint32_t)(b + 1);
+        tm_ok = tm_ok && encode_2d(&L->tm_xq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, rows);
         if (!q2k)
-          tm_ok = tm_ok && encode_2d(&L->tm_hq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, kBoxRows[b]);
+          tm_ok = tm_ok && encode_2d(&L->tm_hq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, rows);
         else
           tm_ok = tm_ok && encode_2d(&L->tm_h16[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.h16, f, pad_rows,
-                                     (uint64_t)f * 2, 64, kBoxRows[b]);
+                                     (uint64_t)f * 2, 64, rows);
       }
       if (!q2k)
         tm_ok = tm_ok && encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn, f, (uint64_t)E * d,
@@ -386,11 +389,15 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int path = path_of(L, T);
   if (path == DS4MOE_PATH_DECODE && !L->s.h_dec) return DS4MOE_ERR_UNSUPPORTED;
-  if (path == DS4MOE_PATH_PREFILL && !L->prefill_ready) return DS4MOE_ERR_UNSUPPORTED;
+  if (path != DS4MOE_PATH_DECODE && !L->prefill_ready) return DS4MOE_ERR_UNSUPPORTED;
+  if (path == DS4MOE_PATH_DECODE_MMA &&
+      2 * (int64_t)T * L->cfg.top_k + (int64_t)L->cfg.n_experts * (kPadRows - 1) > L->s.pad_rows_max)
+    return DS4MOE_ERR_UNSUPPORTED;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != L->device) return DS4MOE_ERR_INVALID_ARG;
 
   L->last_stream = st;
+  const int split = path == DS4MOE_PATH_DECODE_MMA ? 2 : 1;
   int nk = 0;
   auto mark = [&](cudaError_t e) {
     if (e == cudaSuccess && L->timing) e = cudaEventRecord(L->ev[nk], st);
@@ -401,16 +408,16 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   nk = 1;
   if (e == cudaSuccess)
     e = mark(launch_route_topk(L, logits, x, path == DS4MOE_PATH_DECODE, T, st));
-  if (e == cudaSuccess) e = mark(launch_route_group(L, T, st));
+  if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
   if (path == DS4MOE_PATH_DECODE) {
     if (e == cudaSuccess) e = mark(launch_decode_gateup(L, x, out, T, st));
     if (e == cudaSuccess) e = mark(launch_decode_down(L, out, T, st));
   } else {
-    if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, st));
-    if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, st));
+    if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, split, st));
+    if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, split, st));
     if (e == cudaSuccess) {
       if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = mark(launch_gemm_down_q2k(L, out, T, st));
-      else e = mark(launch_gemm_down(L, out, T, st));
+      else e = mark(launch_gemm_down(L, out, T, split, st));
     }
   }
   L->last_nk = nk - 1;
@@ -516,7 +523,7 @@ const char* ds4moe_kernel_name(int path, int i) {
   static const char* dec[] = {"route_topk", "route_group", "decode_gateup", "decode_down"};
   static const char* pre[] = {"route_topk", "route_group", "act_quant", "gemm_gateup", "gemm_down"};
   if (path == DS4MOE_PATH_DECODE && i >= 0 && i < 4) return dec[i];
-  if (path == DS4MOE_PATH_PREFILL && i >= 0 && i < 5) return pre[i];
+  if ((path == DS4MOE_PATH_PREFILL || path == DS4MOE_PATH_DECODE_MMA) && i >= 0 && i < 5) return pre[i];
   return nullptr;
 }
 

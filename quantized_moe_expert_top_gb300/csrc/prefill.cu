@@ -38,9 +38,35 @@ __device__ __forceinline__ size_t act_sf_index(size_t row, int kblk, int r128) {
   return ((size_t)(kblk / 4) * r128 + row / 128) * kSfChunk + (row % 32) * 16 + ((row % 128) / 32) * 4 + (kblk % 4);
 }
 
+// Two E4M3 codes (low byte first) -> their values as f32.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
+  uint32_t h;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "r"(two));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// MXFP8 of one 32-value block: E8M0 exponent s (floor(log2 amax) - 8, clamped;
+// 0 for an all-zero block) and the 32 codes packed little-endian in 8 words.
+__device__ __forceinline__ int mxfp8_block(const float (&v)[32], uint32_t (&packed)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int s = 0;
+  if (amax > 0.f) s = max(-127, min(127, floor_log2_f32(amax) - 8));
+  const float inv = exp2i(-s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
+    const uint32_t hi = f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    packed[i] = lo | (hi << 16);
+  }
+  return s;
+}
+
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k,
                                                         const int32_t* __restrict__ pad_inv, uint8_t* __restrict__ xq,
-                                                        uint8_t* __restrict__ xsf, int r128, float* __restrict__ out) {
+                                                        uint8_t* __restrict__ xsf, int r128, int split,
+                                                        float* __restrict__ out) {
   const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -65,30 +91,35 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
         v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
       }
     }
-    float amax = 0.f;
+    uint32_t packed[8], packed_lo[8];
+    const int s = mxfp8_block(v, packed);
+    int s_lo = 0;
+    if (split == 2) {  // residual after the hi codes, quantised the same way
+      const float sc = exp2i(s);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    int s = 0;
-    if (amax > 0.f) s = max(-127, min(127, floor_log2_f32(amax) - 8));
-    const float inv = exp2i(-s);
-    uint32_t packed[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t lo = f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
-      const uint32_t hi = f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-      packed[i] = lo | (hi << 16);
+      for (int i = 0; i < 8; ++i) {
+        const float2 a = e4m3x2_to_f32x2(packed[i] & 0xFFFFu), b = e4m3x2_to_f32x2(packed[i] >> 16);
+        v[4 * i] -= a.x * sc;
+        v[4 * i + 1] -= a.y * sc;
+        v[4 * i + 2] -= b.x * sc;
+        v[4 * i + 3] -= b.y * sc;
+      }
+      s_lo = mxfp8_block(v, packed_lo);
     }
-    const uint4 c0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    const uint4 c1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    const uint8_t sb = (uint8_t)(s + 127);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k) {
         const size_t r = (size_t)rows[j];
         uint4* dst = reinterpret_cast<uint4*>(xq + r * d + 32 * (size_t)c);
-        dst[0] = c0;
-        dst[1] = c1;
-        xsf[act_sf_index(r, c, r128)] = sb;
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        xsf[act_sf_index(r, c, r128)] = (uint8_t)(s + 127);
+        if (split == 2) {
+          uint4* dlo = reinterpret_cast<uint4*>(xq + (r + 1) * d + 32 * (size_t)c);
+          dlo[0] = make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
+          dlo[1] = make_uint4(packed_lo[4], packed_lo[5], packed_lo[6], packed_lo[7]);
+          xsf[act_sf_index(r + 1, c, r128)] = (uint8_t)(s_lo + 127);
+        }
       }
     }
   }
@@ -152,8 +183,16 @@ struct Cfg<Mode::DownQ2K> {
 constexpr int kAccCol2 = 256;
 constexpr int kSfBase = 448;
 constexpr int kSfSlots = 4;
+// Warps: 0 TMA producer, 1 MMA issuer, then the epilogue warps, the Q2_K
+// dequant warps, and last one helper warp (scale factors / Q2_K chunks by
+// cp.async, L2 prefetch of weight tiles ahead of their TMA load).
 template <Mode M>
-constexpr int threads_of() { return 64 + 32 * Cfg<M>::kEpiWarps + 32 * Cfg<M>::kDeqWarps; }
+constexpr int threads_of() { return 64 + 32 * Cfg<M>::kEpiWarps + 32 * Cfg<M>::kDeqWarps + 32; }
+
+// Token-tile tensor maps, one per box height 16, 32, ..., 192 rows.
+struct alignas(64) BoxMaps {
+  CUtensorMap m[kNumBoxMaps];
+};
 constexpr int kPrefetchStages = 8;     // weight tiles prefetched into L2 ahead of their load
 static_assert(kSfSlots >= Cfg<Mode::GateUp>::kStages && kSfSlots >= Cfg<Mode::Down>::kStages, "scale slots");
 static_assert(kSfBase + kSfSlots * Cfg<Mode::GateUp>::kSfSlot <= 512, "tmem");
@@ -190,6 +229,8 @@ struct GemmArgs {
   const float* topk_w;
   int E, k, d, f;
   const uint8_t* q2k;  // Q2_K down: tile-major chunks
+  const uint8_t* wbase;  // weight rows the A tiles come from (L2 prefetch)
+  int wpitch;
   // outputs
   uint8_t* hq;    // gate/up: MXFP8 h codes [rows][f]
   uint8_t* hsf;   // gate/up: h scales (chunk layout)
@@ -198,6 +239,7 @@ struct GemmArgs {
   DeviceStatus* status;
   uint64_t budget_ns;
   int debug_fault;
+  int split;  // activation rows (token columns) per routed pair: 1, or 2 (hi + lo)
 };
 
 // Work sequence shared by the roles: units u = (expert, 128-row block),
@@ -205,14 +247,15 @@ struct GemmArgs {
 // that start on a 128-token boundary (one chunk when they fit in kNMax).
 struct UnitIter {
   int u, nunits, stride, mb_per_e;
-  int e, mb, ne, t0, nch;
+  int e, mb, ne, t0, nch;  // ne, t0, nch count token columns (split * routed pairs)
   const int32_t* counts;
   int nmax;
+  int split;
   __device__ bool first_chunk() {
     for (; u < nunits; u += stride) {
       e = u / mb_per_e;
       mb = u % mb_per_e;
-      ne = __ldg(counts + e);
+      ne = __ldg(counts + e) * split;
       if (ne > 0) {
         t0 = 0;
         nch = ne <= nmax ? ne : 128;
@@ -254,9 +297,9 @@ struct StageIter {
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 template <Mode M>
-__global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b32,
-    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b128, const GemmArgs args) {
+__global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                                                                       const __grid_constant__ BoxMaps bmaps,
+                                                                       const GemmArgs args) {
   using C = Cfg<M>;
   using S = Smem<M>;
   extern __shared__ uint8_t smem_raw[];
@@ -280,7 +323,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + 32);  // producer (TMA bytes) + helper lanes (cp.async)
       mbar_init(&empty[s], 1);
       mbar_init(&afull[s], C::kDeqWarps > 0 ? C::kDeqWarps : 1);
     }
@@ -292,9 +335,6 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
     *abort_flag = 0;
     fence_barrier_init();
     if (M != Mode::DownQ2K) prefetch_tmap(&tm_a);
-    prefetch_tmap(&tm_b32);
-    prefetch_tmap(&tm_b64);
-    prefetch_tmap(&tm_b128);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -308,23 +348,9 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      StageIter ld{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax},
+      StageIter ld{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split},
                    0, KB, false};
       ld.start();
-      StageIter pf = ld;  // L2 prefetch cursor
-      auto prefetch = [&](const StageIter& p) {
-        const size_t tile = ((size_t)(p.it.e * mb_per_e + p.it.mb) * KB + p.kb);
-        if constexpr (M == Mode::DownQ2K) {
-          bulk_prefetch_l2(args.q2k + tile * kQ2kChunk, kQ2kChunk);
-        } else {
-          tma_prefetch_2d(&tm_a, p.kb * C::kKs, (p.it.e * mb_per_e + p.it.mb) * kBM * C::kNumA);
-          bulk_prefetch_l2(args.sfa + tile * (C::kNumA * kSfChunk), C::kNumA * kSfChunk);
-        }
-      };
-      for (int i = 0; i < kPrefetchStages && pf.valid; ++i) {
-        prefetch(pf);
-        pf.next();
-      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
@@ -336,23 +362,13 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
         const int N = round16(it.nch);
         const int nsf = (N + 127) / 128;
         // token rows in TMA boxes of 128 / 64 / 32 rows (at most two for N <= 192)
-        uint32_t boxes = 0;  // 2 bits per box: 0 = 32 rows, 1 = 64, 2 = 128
-        int nbox = 0, brows = 0;
-        {
-          int rem = N;
-          while (rem >= 128) { boxes |= 2u << (2 * nbox++); rem -= 128; brows += 128; }
-          if (rem > 64) { boxes |= 2u << (2 * nbox++); brows += 128; }
-          else if (rem > 32) { boxes |= 1u << (2 * nbox++); brows += 64; }
-          else if (rem > 0) { nbox++; brows += 32; }
-        }
+        const CUtensorMap* tb = &bmaps.m[N / 16 - 1];  // one box of exactly N token rows
         const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
         const int arow = (it.e * mb_per_e + it.mb) * kBM * C::kNumA;  // gate+up: 256-row box
         // A 4-bit unpacking load counts its packed global bytes (half the
         // 16 KB it writes to shared memory).
-        const uint32_t bytes = M == Mode::DownQ2K
-                                   ? (uint32_t)(brows * 128 + kQ2kChunk)
-                                   : (uint32_t)(C::kNumA * S::kA / 2 + brows * 128 + (C::kNumA + nsf) * kSfChunk);
-        const size_t tile0 = (size_t)(it.e * mb_per_e + it.mb) * KB;
+        const uint32_t bytes = (uint32_t)((M == Mode::DownQ2K ? 0 : C::kNumA * S::kA / 2) + N * 128);
+        (void)nsf;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
@@ -362,36 +378,18 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
           }
           uint8_t* st = smem + stage * S::kStage;
           uint8_t* sb = st + C::kNumA * S::kA;
-          uint8_t* ssf = sb + S::kB;
           mbar_arrive_expect_tx(&full[stage], bytes);
           if (fault_pending) {
             fault_pending = false;  // test-only: drop this stage's loads
           } else {
-            int r = 0;
-            for (int i = 0; i < nbox; ++i) {
-              const uint32_t bx = (boxes >> (2 * i)) & 3u;
-              const CUtensorMap* tb = bx == 2 ? &tm_b128 : (bx == 1 ? &tm_b64 : &tm_b32);
-              tma_load_2d(sb + r * 128, tb, &full[stage], kb * C::kKs, prow + r);
-              r += 32 << bx;
-            }
-            if constexpr (M == Mode::DownQ2K) {
-              bulk_load(ssf, args.q2k + (tile0 + kb) * kQ2kChunk, kQ2kChunk, &full[stage]);
-            } else {
-              tma_load_2d(st, &tm_a, &full[stage], kb * C::kKs, arow);
-              bulk_load(ssf, args.sfa + (tile0 + kb) * (C::kNumA * kSfChunk), C::kNumA * kSfChunk, &full[stage]);
-              bulk_load(ssf + C::kNumA * kSfChunk, args.sfb + ((size_t)kb * args.r128 + prow / 128) * kSfChunk,
-                        nsf * kSfChunk, &full[stage]);
-            }
+            tma_load_2d(sb, tb, &full[stage], kb * C::kKs, prow);
+            if constexpr (M != Mode::DownQ2K) tma_load_2d(st, &tm_a, &full[stage], kb * C::kKs, arow);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
-          }
-          if (pf.valid) {
-            prefetch(pf);
-            pf.next();
           }
         }
       }
@@ -408,7 +406,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
+      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split};
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;  // acc_phase bit b: phase of accumulator buffer b
       uint32_t sf_seq = 0;  // running stage count; slot = sf_seq % kSfSlots (kSfSlots >= kStages)
@@ -460,6 +458,8 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
             for (int j = 0; j < 4; ++j)  // K = 16 fp16 (32 bytes) per instruction
               mma_f16(acc0, ad + 2 * j, bd + 2 * j, idesc0, (kb > 0 || j > 0) ? 1u : 0u);
           } else {
+            // the scale factors were written by cp.async (generic proxy); tcgen05.cp reads through the async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint32_t slot = tmem + kSfBase + (sf_seq++ % kSfSlots) * C::kSfSlot;
             // scale factors -> tensor memory: A chunk(s) at slot+0 (+4), B chunks after (512 B = 32 units)
             const uint64_t sd = sfdesc0 + soff;
@@ -489,11 +489,71 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
       mbar_wait_bounded(drain, 0, args.budget_ns, &never);
     }
     __syncwarp();
+  } else if (warp == threads_of<M>() / 32 - 1) {
+    // ------------------------------------------------------------ helper: scale factors / Q2_K chunks
+    StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split},
+                 0, KB, false};
+    sq.start();
+    StageIter pf = sq;  // L2 prefetch cursor, kPrefetchStages ahead
+    auto l2_prefetch = [&](const StageIter& p) {
+      const size_t tile = (size_t)(p.it.e * mb_per_e + p.it.mb) * KB + p.kb;
+      if constexpr (M == Mode::DownQ2K) {
+        if (lane < kQ2kChunk / 128) prefetch_l2(args.q2k + tile * kQ2kChunk + lane * 128);
+      } else {
+        const int arow = (p.it.e * mb_per_e + p.it.mb) * kBM * C::kNumA;
+        for (int r = lane; r < kBM * C::kNumA; r += 32)
+          prefetch_l2(args.wbase + (size_t)(arow + r) * args.wpitch + p.kb * (C::kKs / 2));
+        if (lane < C::kNumA * kSfChunk / 128) prefetch_l2(args.sfa + tile * (C::kNumA * kSfChunk) + lane * 128);
+      }
+    };
+    for (int i = 0; i < kPrefetchStages && pf.valid; ++i) {
+      l2_prefetch(pf);
+      pf.next();
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    while (sq.valid) {
+      uint32_t got = 0;
+      if (lane == 0) got = mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag) ? 1u : 0u;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) {
+          report_timeout(args.status, kWhereProducerEmpty);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      uint8_t* ssf = smem + stage * S::kStage + C::kNumA * S::kA + S::kB;
+      const size_t tile = (size_t)(sq.it.e * mb_per_e + sq.it.mb) * KB + sq.kb;
+      if constexpr (M == Mode::DownQ2K) {
+        const uint8_t* src = args.q2k + tile * kQ2kChunk;
+        for (int i = lane; i < kQ2kChunk / 16; i += 32) cp_async_16(ssf + 16 * i, src + 16 * i);
+      } else {
+        const int N = round16(sq.it.nch);
+        const int nA = C::kNumA * kSfChunk / 16, nB = ((N + 127) / 128) * kSfChunk / 16;
+        const int prow = __ldg(args.pad_offsets + sq.it.e) + sq.it.t0;
+        const uint8_t* sfa = args.sfa + tile * (C::kNumA * kSfChunk);
+        const uint8_t* sfb = args.sfb + ((size_t)sq.kb * args.r128 + prow / 128) * kSfChunk;
+        for (int i = lane; i < nA + nB; i += 32)
+          cp_async_16(ssf + 16 * i, i < nA ? sfa + 16 * i : sfb + 16 * (i - nA));
+      }
+      cp_async_arrive_noinc(&full[stage]);
+      if (pf.valid) {
+        l2_prefetch(pf);
+        pf.next();
+      }
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      sq.next();
+    }
+    cp_async_wait_all();  // this warp's copies land before the CTA may exit
   } else if (warp >= 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ Q2_K dequant
     if constexpr (M == Mode::DownQ2K) {
       const int r = (warp - 2 - C::kEpiWarps) * 32 + lane;  // weight row of the 128-row tile
-      StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax},
+      StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split},
                    0, KB, false};
       sq.start();
       int stage = 0;
@@ -557,7 +617,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
     constexpr int kParts = C::kEpiWarps / 4;
     const int etid = threadIdx.x - 64;  // index among the epilogue threads
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax};
+    UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split};
     uint32_t acc_phase = 0;
     int chunk = 0;
     for (bool more = it.first_chunk(); more; more = it.next(), ++chunk) {
@@ -611,6 +671,35 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
           tmem_ld_32x32b_x16(acc0 + (uint32_t)(kAccCol2 + c0), r1);
           tmem_ld_wait();
           const int i = unit_row;  // feature index in [0, f)
+          if (args.split == 2) {
+            // column pairs (hi, lo) of 8 tokens: add them, SwiGLU, then h -> hi + lo rows again
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float g = __uint_as_float(r0[2 * jj]) + __uint_as_float(r0[2 * jj + 1]);
+              const float u = __uint_as_float(r1[2 * jj]) + __uint_as_float(r1[2 * jj + 1]);
+              const float h = __fdividef(g, 1.f + __expf(-g)) * u;
+              const float a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+              int s = 0;
+              if (a > 0.f) s = max(-127, min(127, floor_log2_f32(a) - 8));
+              const uint32_t chi = f32x2_to_e4m3x2(h * exp2i(-s), 0.f) & 0xFFu;
+              const float res = h - e4m3x2_to_f32x2(chi).x * exp2i(s);
+              const float a2 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(res))));
+              int s2 = 0;
+              if (a2 > 0.f) s2 = max(-127, min(127, floor_log2_f32(a2) - 8));
+              const uint32_t clo = f32x2_to_e4m3x2(res * exp2i(-s2), 0.f) & 0xFFu;
+              const int col = c0 + 2 * jj;
+              if (col < it.nch) {
+                const size_t row = (size_t)(prow + col);
+                args.hq[row * args.f + i] = (uint8_t)chi;
+                args.hq[(row + 1) * args.f + i] = (uint8_t)clo;
+                if (lane == 0) {
+                  args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
+                  args.hsf[act_sf_index(row + 1, i / 32, args.r128)] = (uint8_t)(s2 + 127);
+                }
+              }
+            }
+            continue;
+          }
           float h[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
@@ -641,11 +730,21 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
         } else {
           tmem_ld_wait();
           const int m = unit_row;  // output feature
+          if (args.split == 2) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int col = c0 + jj;
-            if (col < it.nch)
-              red_add_f32(args.out + (size_t)col_tok[col] * args.d + m, col_w[col] * __uint_as_float(r0[jj]));
+            for (int jj = 0; jj < 8; ++jj) {
+              const int col = c0 + 2 * jj;
+              if (col < it.nch)
+                red_add_f32(args.out + (size_t)col_tok[col] * args.d + m,
+                            col_w[col] * (__uint_as_float(r0[2 * jj]) + __uint_as_float(r0[2 * jj + 1])));
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = c0 + jj;
+              if (col < it.nch)
+                red_add_f32(args.out + (size_t)col_tok[col] * args.d + m, col_w[col] * __uint_as_float(r0[jj]));
+            }
           }
         }
       }
@@ -666,22 +765,25 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(
 template <Mode M>
 cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a, const CUtensorMap* b, const GemmArgs& args,
                         cudaStream_t st) {
+  BoxMaps maps;
+  for (int i = 0; i < kNumBoxMaps; ++i) maps.m[i] = b[i];
   static_assert(Smem<M>::kTotal <= 227 * 1024, "shared memory");
   const void* fn = (const void*)grouped_gemm_kernel<M>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<M>::kTotal);
   if (e != cudaSuccess) return e;
   const int units = args.E * (args.rows_per_expert / kBM);
   const int grid = units < L->num_sms ? units : L->num_sms;
-  grouped_gemm_kernel<M><<<grid, threads_of<M>(), Smem<M>::kTotal, st>>>(a, b[0], b[1], b[2], args);
+  grouped_gemm_kernel<M><<<grid, threads_of<M>(), Smem<M>::kTotal, st>>>(a, maps, args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st) {
+cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, int split, cudaStream_t st) {
   const int blocks = (T + 7) / 8;
   act_quant_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T, L->cfg.d_model, L->cfg.top_k,
-                                           L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), out);
+                                           L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), split,
+                                           out);
   return cudaGetLastError();
 }
 
@@ -698,14 +800,18 @@ static GemmArgs base_args(const ds4moe_layer* L) {
   a.status = L->status;
   a.r128 = (int)(L->s.pad_rows_max / 128);
   a.debug_fault = L->cfg.debug_fault;
+  a.split = 1;
   a.budget_ns = L->cfg.debug_fault ? 1000000ull : (uint64_t)L->cfg.wait_timeout_ms * 1000000ull;
   return a;
 }
 
-cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, cudaStream_t st) {
+cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStream_t st) {
   (void)T;
   GemmArgs a = base_args(L);
+  a.split = split;
   a.sfa = L->w.gu_sf;
+  a.wbase = L->w.gu;
+  a.wpitch = L->w.pitch_gu;
   a.rows_per_expert = L->cfg.d_ff;
   a.K = L->cfg.d_model;
   a.sfb = L->s.xsf;
@@ -715,11 +821,14 @@ cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, cudaStream_t st) {
   return launch_gemm<Mode::GateUp>(L, L->tm_gu, L->tm_xq, a, st);
 }
 
-cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
+cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st) {
   (void)T;
   GemmArgs a = base_args(L);
+  a.split = split;
   a.debug_fault = 0;
   a.sfa = L->w.down_sf;
+  a.wbase = L->w.dn;
+  a.wpitch = L->w.pitch_dn;
   a.rows_per_expert = L->cfg.d_model;
   a.K = L->cfg.d_ff;
   a.sfb = L->s.hsf;

@@ -156,7 +156,8 @@ __device__ __forceinline__ int block_scan_incl(int v, int* warp_tot) {
 
 // Grid = E blocks of 256 threads; block e places expert e's pairs.
 //   offsets[e]     = number of pairs with expert < e (exclusive scan of counts)
-//   pad_offsets[e] = same over counts rounded up to 128 rows
+//   pad_offsets[e] = same over rpp*counts rounded up to 128 rows (rpp = padded
+//                    rows per pair: 1, or 2 when x is split into hi + lo rows)
 //   rank of pair (t, j) with idx[t,j] == e = number of tokens t' < t that
 //   selected e (each token selects an expert at most once), so the order is
 //   (expert, token) and is independent of thread timing.
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ perm_slot, int32_t* __restrict__ inv,
                                                           int32_t* __restrict__ pad_inv,
                                                           int32_t* __restrict__ pad_pair,
-                                                          int32_t* __restrict__ touched) {
+                                                          int32_t* __restrict__ touched, int rpp) {
   __shared__ int hist[kMaxE];
   __shared__ int warp_tot[32];
   __shared__ int s_off, s_poff;
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
 
   // exclusive scans of counts, padded counts and the touched flag (tid = expert)
   const int c = (tid < E) ? hist[tid] : 0;
-  const int pc = (c + kPadRows - 1) / kPadRows * kPadRows;
+  const int pc = (c * rpp + kPadRows - 1) / kPadRows * kPadRows;
   const int inc_c = block_scan_incl(c, warp_tot);
   const int inc_pc = block_scan_incl(pc, warp_tot);
   const int inc_t = block_scan_incl(c > 0 ? 1 : 0, warp_tot);
@@ -226,13 +227,13 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
     }
     if (slot >= 0) {
       const int r = running + before + in_warp;
-      const int pos = off + r, ppos = poff + r;
+      const int pos = off + r, ppos = poff + r * rpp;
       const int pair = t * k + slot;
       perm_tok[pos] = t;
       perm_slot[pos] = slot;
       inv[pair] = pos;
       pad_inv[pair] = ppos;
-      pad_pair[ppos] = pair;
+      for (int q = 0; q < rpp; ++q) pad_pair[ppos + q] = pair;
     }
     running += total;
     __syncthreads();
@@ -252,11 +253,11 @@ cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_group(const ds4moe_layer* L, int T, cudaStream_t st) {
+cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream_t st) {
   const int E = L->cfg.n_experts, k = L->cfg.top_k;
   const Scratch& s = L->s;
   route_group_kernel<<<E, 256, 0, st>>>(s.topk_idx, T, E, k, s.counts, s.offsets, s.pad_offsets, s.perm_tok,
-                                        s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched);
+                                        s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, rpp);
   return cudaGetLastError();
 }
 
@@ -334,7 +335,7 @@ extern "C" int ds4moe_route_noalloc(const float* logits, int32_t T, int32_t E, i
   const int blocks = (T + 7) / 8;
   route_topk_kernel<<<blocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, nullptr, 0, nullptr, nullptr);
   route_group_kernel<<<E, 256, 0, st>>>(topk_idx, T, E, k, counts, offsets, pad_offsets, perm_tok, perm_slot, inv,
-                                        pad_inv, pad_pair, touched);
+                                        pad_inv, pad_pair, touched, 1);
   if (cudaGetLastError() != cudaSuccess) return DS4MOE_ERR_CUDA;
   return DS4MOE_OK;
 }

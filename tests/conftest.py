@@ -40,8 +40,10 @@ def big_layer(ds4):
     W = synth.make_layer_weights(wl, device="cuda")
     torch.cuda.synchronize()
     Wh = {k: v.cpu().numpy() for k, v in W.items()}
-    layer = ds4.Layer(wl.d, wl.E, wl.f, wl.k, 4096, W)
+    layer = ds4.Layer(wl.d, wl.E, wl.f, wl.k, 4096, W)           # AUTO: DECODE_MMA for T <= 64, else PREFILL
+    gemv = ds4.Layer(wl.d, wl.E, wl.f, wl.k, 64, W, force_path="decode")  # the CUDA-core GEMV decode path
     del W
     torch.cuda.empty_cache()
-    yield {"wl": wl, "Wh": Wh, "layer": layer}
+    yield {"wl": wl, "Wh": Wh, "layer": layer, "gemv": gemv}
     layer.close()
+    gemv.close()

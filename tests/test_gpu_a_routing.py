@@ -18,7 +18,7 @@ def _routing_layer(ds4, wl, T, path):
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode1", "decode64", "prefill", "q2k"])
-@pytest.mark.parametrize("path", ["decode", "prefill"])
+@pytest.mark.parametrize("path", ["decode", "decode_mma", "prefill"])
 def test_routing_matches_oracle(ds4, name, path):
     wl = synth.WORKLOADS[name]
     logits = synth.make_logits(wl, device="cuda")

@@ -1,4 +1,6 @@
-"""Decode (few-token) path vs the oracle in its exact-activation mode."""
+"""Few-token decode paths vs the oracle in its exact-activation mode: the
+CUDA-core GEMV path (forced) and the split-precision tensor-core path
+(DECODE_MMA, the default for T <= 64)."""
 import numpy as np
 import pytest
 import torch
@@ -21,24 +23,26 @@ def _run(ds4, wl, path, T=None):
     out = layer.forward(inp["x"], inp["logits"])
     torch.cuda.synchronize()
     assert layer.status() == ds4.OK
-    act = oracle.ACT_EXACT if path == "decode" else oracle.ACT_MXFP8
+    act = oracle.ACT_MXFP8 if path == "prefill" else oracle.ACT_EXACT
     idx, w = oracle.route(inp["logits"].cpu().numpy(), wl.k)
     ref = oracle.forward(dims_of(wl), host_weights(W), bf16_bits(inp["x"]), idx, w, list(range(T)), act)
     layer.close()
     return out.cpu().numpy(), ref
 
 
+@pytest.mark.parametrize("path", ["decode", "decode_mma"])
 @pytest.mark.parametrize("wl", [synth.WORKLOADS["tiny"], MID, UNIT], ids=lambda w: w.name)
-def test_decode_path_full_parity(ds4, wl):
-    out, ref = _run(ds4, wl, "decode")
-    assert_parity(out, ref, wl.name)
+def test_decode_paths_full_parity(ds4, wl, path):
+    out, ref = _run(ds4, wl, path)
+    assert_parity(out, ref, f"{wl.name} {path}")
 
 
-def test_decode_one_token_full_size(ds4, big_layer):
+@pytest.mark.parametrize("which", ["layer", "gemv"])
+def test_decode_one_token_full_size(ds4, big_layer, which):
     wl = synth.WORKLOADS["decode1"]
-    layer = big_layer["layer"]
+    layer = big_layer[which]
     inp = synth.make_inputs(wl, device="cuda")
-    assert layer.path_for(1) == ds4.PATH_DECODE
+    assert layer.path_for(1) == (ds4.PATH_DECODE_MMA if which == "layer" else ds4.PATH_DECODE)
     out = layer.forward(inp["x"], inp["logits"])
     torch.cuda.synchronize()
     assert layer.status() == ds4.OK
@@ -47,11 +51,12 @@ def test_decode_one_token_full_size(ds4, big_layer):
     assert_parity(out.cpu().numpy(), ref, "decode1")
 
 
-def test_decode_64_tokens_zipf_full_size(ds4, big_layer):
+@pytest.mark.parametrize("which", ["layer", "gemv"])
+def test_decode_64_tokens_zipf_full_size(ds4, big_layer, which):
     wl = synth.WORKLOADS["decode64"]
-    layer = big_layer["layer"]
+    layer = big_layer[which]
     inp = synth.make_inputs(wl, device="cuda")
-    assert layer.path_for(64) == ds4.PATH_DECODE
+    assert layer.path_for(64) == (ds4.PATH_DECODE_MMA if which == "layer" else ds4.PATH_DECODE)
     out = layer.forward(inp["x"], inp["logits"])
     torch.cuda.synchronize()
     assert layer.status() == ds4.OK

@@ -30,10 +30,11 @@ def test_q2k_full_parity(ds4, wl):
     layer.close()
 
 
-def test_q2k_decode_path_is_rejected(ds4):
+@pytest.mark.parametrize("path", ["decode", "decode_mma"])
+def test_q2k_decode_paths_are_rejected(ds4, path):
     W = synth.make_layer_weights(TINY_Q2K, device="cuda")
     with pytest.raises(ds4.Ds4moeError) as ei:
-        ds4.Layer(TINY_Q2K.d, TINY_Q2K.E, TINY_Q2K.f, TINY_Q2K.k, 6, W, force_path="decode")
+        ds4.Layer(TINY_Q2K.d, TINY_Q2K.E, TINY_Q2K.f, TINY_Q2K.k, 6, W, force_path=path)
     assert ei.value.code == ds4.ERR_UNSUPPORTED
 
 

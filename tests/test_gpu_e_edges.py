@@ -51,10 +51,10 @@ def test_misaligned_pointer_rejected(ds4, tiny):
 
 def test_path_choice_and_launch_counts(ds4, tiny):
     _, _, layer = tiny
-    assert layer.path_for(4) == ds4.PATH_DECODE
+    assert layer.path_for(4) == ds4.PATH_DECODE_MMA
     assert layer.path_for(5) == ds4.PATH_PREFILL
     assert layer.path_for(17) == ds4.ERR_TOO_MANY_TOKENS
-    assert layer.launches_per_forward(4) == 4
+    assert layer.launches_per_forward(4) == 5
     assert layer.launches_per_forward(16) == 5
 
 
@@ -65,7 +65,7 @@ def test_host_call_matches_device_call(ds4, tiny, T):
     out_h = layer.forward_host(inp["x"].pin_memory(), inp["logits"].pin_memory())
     out_d = layer.forward(inp["x"].cuda(), inp["logits"].cuda()).cpu()
     assert torch.allclose(out_h, out_d, rtol=1e-5, atol=1e-6)
-    act = oracle.ACT_EXACT if T <= 4 else oracle.ACT_MXFP8
+    act = oracle.ACT_EXACT if T <= 4 else oracle.ACT_MXFP8  # T <= 4: DECODE_MMA (exact-activation mode)
     idx, w = oracle.route(inp["logits"].numpy(), wl.k)
     ref = oracle.forward(dims_of(wl), host_weights(W), bf16_bits(inp["x"]), idx, w, list(range(T)), act)
     assert_parity(out_h.numpy(), ref, f"host T={T}")
@@ -76,7 +76,7 @@ def test_layer_at_max_tokens_both_paths(ds4):
     W = synth.make_layer_weights(wl, device="cuda")
     inp = synth.make_inputs(wl, device="cuda")
     idx, w = oracle.route(inp["logits"].cpu().numpy(), wl.k)
-    for path, act in (("decode", oracle.ACT_EXACT), ("prefill", oracle.ACT_MXFP8)):
+    for path, act in (("decode", oracle.ACT_EXACT), ("decode_mma", oracle.ACT_EXACT), ("prefill", oracle.ACT_MXFP8)):
         layer = ds4.Layer(wl.d, wl.E, wl.f, wl.k, 33, W, force_path=path)
         out = layer.forward(inp["x"], inp["logits"])
         torch.cuda.synchronize()
