@@ -80,6 +80,22 @@ def workload_accounting(wl: synth.Workload, counts: np.ndarray) -> dict:
     }
 
 
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel source changed since those counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as fh:
+            rec = json.load(fh)
+        src = os.path.join(ROOT, "quantized_moe_expert_top_gb300", "csrc", "prefill.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != rec.get("prefill_cu_sha256_16"):
+            return None
+        return rec.get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -297,7 +313,8 @@ def run_ours(args):
         else:
             roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"]}
-        roofline.update({"kernel": dom, "kernel_ms": kms[dom], "traffic": None,
+        roofline.update({"kernel": dom, "kernel_ms": kms[dom],
+                         "traffic": measured_traffic(dom) if wl.name == "prefill" else None,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                          else "fallback",
                          "algorithmic_bytes": acc[bytes_key[dom]], "algorithmic_flops": acc[flops_key[dom]]})
