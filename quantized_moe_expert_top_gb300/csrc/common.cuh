@@ -172,6 +172,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of a forward is launched with programmatic stream
+// serialisation: it may start while the previous kernel drains.  pdl_wait()
+// blocks until that kernel has completed and its writes are visible, so it
+// comes before the first access to global memory that another kernel of the
+// chain writes or reads; pdl_launch_dependents() lets the next kernel start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y) {
   asm volatile(

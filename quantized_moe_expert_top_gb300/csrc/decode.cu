@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
     float* __restrict__ out, int T, int d, int f, const int32_t* __restrict__ touched,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_tok, float* __restrict__ h_dec, int E,
     DeviceStatus* status, uint64_t budget) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
@@ -265,6 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(
     const int32_t* __restrict__ touched, const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_tok,
     const int32_t* __restrict__ perm_slot, const float* __restrict__ topk_w, const float* __restrict__ h_dec, int E,
     DeviceStatus* status, uint64_t budget) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_s;
   volatile int* abort_flag = &abort_s;
@@ -357,10 +361,9 @@ cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* ou
   const size_t smem = ring_smem(2 * kConsumers * L->w.pitch_gu);
   cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_gateup_kernel<<<L->num_sms, kThreads, smem, st>>>(
-      L->w.gu, L->w.pitch_gu, reinterpret_cast<const uint4*>(L->s.xh), L->s.xsig, out, T, d, f, L->s.touched,
-      L->s.offsets, L->s.perm_tok, L->s.h_dec, E, L->status, (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
-  return cudaGetLastError();
+  return launch_pdl(decode_gateup_kernel, L->num_sms, kThreads, smem, st, L->w.gu, L->w.pitch_gu,
+                    reinterpret_cast<const uint4*>(L->s.xh), L->s.xsig, out, T, d, f, L->s.touched, L->s.offsets,
+                    L->s.perm_tok, L->s.h_dec, E, L->status, (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
 }
 
 cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
@@ -369,10 +372,9 @@ cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStr
   const size_t smem = ring_smem(kConsumers * kDnRowsPerWarp * L->w.pitch_dn);
   cudaError_t e = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_down_kernel<<<L->num_sms, kThreads, smem, st>>>(
-      L->w.dn, L->w.pitch_dn, out, d, f, k, L->s.touched, L->s.offsets, L->s.perm_tok, L->s.perm_slot, L->s.topk_w,
-      L->s.h_dec, E, L->status, (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
-  return cudaGetLastError();
+  return launch_pdl(decode_down_kernel, L->num_sms, kThreads, smem, st, L->w.dn, L->w.pitch_dn, out, d, f, k,
+                    L->s.touched, L->s.offsets, L->s.perm_tok, L->s.perm_slot, L->s.topk_w, L->s.h_dec, E, L->status,
+                    (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
 }
 
 int decode_launches() { return 4; }

@@ -12,6 +12,25 @@ namespace ds4moe {
 
 struct DeviceStatus;
 
+// Launches `kernel` on `st` with programmatic stream serialisation, so that
+// its blocks can be scheduled while the previous kernel in the stream drains
+// (each kernel waits with griddepcontrol.wait before touching shared data).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Tile geometry of the prefill GEMMs.
 constexpr int kBM = 128;          // rows of a weight tile (tcgen05 M)
 constexpr int kBK = 128;          // contraction elements per pipeline stage

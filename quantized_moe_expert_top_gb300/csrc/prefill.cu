@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
                                                         const int32_t* __restrict__ pad_inv, uint8_t* __restrict__ xq,
                                                         uint8_t* __restrict__ xsf, int r128, int split,
                                                         float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -224,6 +226,7 @@ struct GemmArgs {
   const uint8_t* sfb;   // chunk-layout scales of the B rows
   // routing
   const int32_t* counts;
+  const int32_t* touched;  // experts with tokens, ascending, then their number at [E]
   const int32_t* pad_offsets;
   const int32_t* pad_pair;
   const float* topk_w;
@@ -242,18 +245,20 @@ struct GemmArgs {
   int split;  // activation rows (token columns) per routed pair: 1, or 2 (hi + lo)
 };
 
-// Work sequence shared by the roles: units u = (expert, 128-row block),
-// expert-major, strided over the CTAs; each unit's tokens split into chunks
-// that start on a 128-token boundary (one chunk when they fit in kNMax).
+// Work sequence shared by the roles: units u = (touched expert, 128-row
+// block), expert-major, strided over the CTAs, so that units are dealt evenly
+// whatever experts the tokens chose; each unit's tokens split into chunks that
+// start on a 128-token boundary (one chunk when they fit in kNMax).
 struct UnitIter {
   int u, nunits, stride, mb_per_e;
   int e, mb, ne, t0, nch;  // ne, t0, nch count token columns (split * routed pairs)
   const int32_t* counts;
+  const int32_t* touched;
   int nmax;
   int split;
   __device__ bool first_chunk() {
     for (; u < nunits; u += stride) {
-      e = u / mb_per_e;
+      e = __ldg(touched + u / mb_per_e);
       mb = u % mb_per_e;
       ne = __ldg(counts + e) * split;
       if (ne > 0) {
@@ -318,7 +323,6 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mb_per_e = args.rows_per_expert / kBM;
-  const int nunits = args.E * mb_per_e;
   const int KB = args.K / C::kKs;
 
   if (threadIdx.x == 0) {
@@ -344,11 +348,14 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the routing tables and activations of this forward are complete from here on
+  pdl_launch_dependents();
+  const int nunits = __ldg(args.touched + args.E) * mb_per_e;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      StageIter ld{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split},
+      StageIter ld{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched, C::kNMax, args.split},
                    0, KB, false};
       ld.start();
       int stage = 0;
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split};
+      UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched, C::kNMax, args.split};
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;  // acc_phase bit b: phase of accumulator buffer b
       uint32_t sf_seq = 0;  // running stage count; slot = sf_seq % kSfSlots (kSfSlots >= kStages)
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
     __syncwarp();
   } else if (warp == threads_of<M>() / 32 - 1) {
     // ------------------------------------------------------------ helper: scale factors / Q2_K chunks
-    StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split},
+    StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched, C::kNMax, args.split},
                  0, KB, false};
     sq.start();
     StageIter pf = sq;  // L2 prefetch cursor, kPrefetchStages ahead
@@ -553,7 +560,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
     // ------------------------------------------------------------ Q2_K dequant
     if constexpr (M == Mode::DownQ2K) {
       const int r = (warp - 2 - C::kEpiWarps) * 32 + lane;  // weight row of the 128-row tile
-      StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split},
+      StageIter sq{{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched, C::kNMax, args.split},
                    0, KB, false};
       sq.start();
       int stage = 0;
@@ -617,7 +624,7 @@ __global__ void __launch_bounds__(threads_of<M>(), 1) grouped_gemm_kernel(const 
     constexpr int kParts = C::kEpiWarps / 4;
     const int etid = threadIdx.x - 64;  // index among the epilogue threads
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, C::kNMax, args.split};
+    UnitIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched, C::kNMax, args.split};
     uint32_t acc_phase = 0;
     int chunk = 0;
     for (bool more = it.first_chunk(); more; more = it.next(), ++chunk) {
@@ -773,23 +780,21 @@ cudaError_t launch_gemm(const ds4moe_layer* L, const CUtensorMap& a, const CUten
   if (e != cudaSuccess) return e;
   const int units = args.E * (args.rows_per_expert / kBM);
   const int grid = units < L->num_sms ? units : L->num_sms;
-  grouped_gemm_kernel<M><<<grid, threads_of<M>(), Smem<M>::kTotal, st>>>(a, maps, args);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<M>, grid, threads_of<M>(), Smem<M>::kTotal, st, a, maps, args);
 }
 
 }  // namespace
 
 cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, int split, cudaStream_t st) {
   const int blocks = (T + 7) / 8;
-  act_quant_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T, L->cfg.d_model, L->cfg.top_k,
-                                           L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), split,
-                                           out);
-  return cudaGetLastError();
+  return launch_pdl(act_quant_kernel, blocks, 256, 0, st, static_cast<const __nv_bfloat16*>(x), T, L->cfg.d_model,
+                    L->cfg.top_k, L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), split, out);
 }
 
 static GemmArgs base_args(const ds4moe_layer* L) {
   GemmArgs a{};
   a.counts = L->s.counts;
+  a.touched = L->s.touched;
   a.pad_offsets = L->s.pad_offsets;
   a.pad_pair = L->s.pad_pair;
   a.topk_w = L->s.topk_w;

@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int32_t* __restrict__ idx, float* __restrict__ w,
                                                          const __nv_bfloat16* __restrict__ x, int d,
                                                          uint4* __restrict__ xh, float* __restrict__ xsig) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int token = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
@@ -172,6 +174,8 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   __shared__ int hist[kMaxE];
   __shared__ int warp_tot[32];
   __shared__ int s_off, s_poff;
+  pdl_wait();
+  pdl_launch_dependents();
   const int e = blockIdx.x;
   const int tid = threadIdx.x;
   const int npairs = T * k;
@@ -246,19 +250,16 @@ cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const 
                               cudaStream_t st) {
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
-  route_topk_kernel<<<blocks, 32 * warps_per_block, 0, st>>>(
-      logits, T, L->cfg.n_experts, L->cfg.top_k, L->s.topk_idx, L->s.topk_w,
-      static_cast<const __nv_bfloat16*>(x), L->cfg.d_model, prep_x ? reinterpret_cast<uint4*>(L->s.xh) : nullptr,
-      L->s.xsig);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel, blocks, 32 * warps_per_block, 0, st, logits, T, L->cfg.n_experts,
+                    L->cfg.top_k, L->s.topk_idx, L->s.topk_w, static_cast<const __nv_bfloat16*>(x), L->cfg.d_model,
+                    prep_x ? reinterpret_cast<uint4*>(L->s.xh) : nullptr, L->s.xsig);
 }
 
 cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream_t st) {
   const int E = L->cfg.n_experts, k = L->cfg.top_k;
   const Scratch& s = L->s;
-  route_group_kernel<<<E, 256, 0, st>>>(s.topk_idx, T, E, k, s.counts, s.offsets, s.pad_offsets, s.perm_tok,
-                                        s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, rpp);
-  return cudaGetLastError();
+  return launch_pdl(route_group_kernel, E, 256, 0, st, s.topk_idx, T, E, k, s.counts, s.offsets, s.pad_offsets,
+                    s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, rpp);
 }
 
 }  // namespace ds4moe
