@@ -158,7 +158,7 @@ __device__ Ring setup_ring(uint8_t* smem_raw, int stage_bytes) {
 // Rows = every (gate row i, up row i) pair of every touched expert; stage =
 // kConsumers gate rows then their kConsumers up rows, one pair per consumer
 // warp.  In the tile-major weight layout gate row i of expert e is row
-// (e*f/128 + i/128)*256 + i%128, its up row 128 rows later.
+// (e*f/64 + i/64)*128 + i%64, its up row 64 rows later.
 __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
     const uint8_t* __restrict__ gu, int pitch, const uint4* __restrict__ xh, const float* __restrict__ xsig,
     float* __restrict__ out, int T, int d, int f, const int32_t* __restrict__ touched,
@@ -186,9 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(
           R, r0, r1, kConsumers, pitch,
           [&](int r) {
             const int i = r % f;
-            return gu + (((size_t)__ldg(touched + r / f) * (f / 128) + i / 128) * 256 + i % 128) * pitch;
+            return gu + (((size_t)__ldg(touched + r / f) * (f / 64) + i / 64) * 128 + i % 64) * pitch;
           },
-          true, (size_t)128 * pitch, budget, status, abort_flag);
+          true, (size_t)64 * pitch, budget, status, abort_flag);
     return;
   }
   const int cw = warp - 1;

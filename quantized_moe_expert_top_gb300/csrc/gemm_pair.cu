@@ -1,0 +1,602 @@
+// Grouped block-scaled GEMMs of the routed experts on CTA pairs
+// (tcgen05 cta_group::2): gate/up with the SwiGLU + MXFP8 epilogue, and down
+// with the weighted combine back into token order.
+//
+// "DwarfStar実地分析" §GGUFの対応範囲は意図的に狭い states that on Blackwell CUDA
+// the batched expert work runs on FP4 matrix instructions.  Every expert's
+// tokens form one GEMM with the weights as the M side (swap-AB): the E2M1
+// weights are A (TMA expands the packed nibbles into the 16-byte-aligned layout
+// the MMA reads), the E4M3 activations of the expert's tokens are B, with one
+// E8M0 scale per 32 K on both, accumulated in fp32 in tensor memory.
+//
+// Two CTAs of a cluster form a pair and issue one M = 256 MMA: each CTA holds
+// 128 weight rows and half of the token rows in its shared memory, and the
+// leader (rank 0) issues the MMAs for both.  Each weight and token byte is
+// written to and read from shared memory once per pair, which is what bounds a
+// single CTA's tile rate, and the smaller stage leaves room for seven stages.
+//
+//   gate/up : the pair covers 128 features of one expert; each CTA's 128 rows
+//             are the gate rows then the up rows of its 64 features, so its
+//             accumulator holds g in lanes 0..63 and u in lanes 64..127 for
+//             every token.  The gate warps stage silu(g) in shared memory for
+//             the up warps, which form h = silu(g) * u and quantise it to
+//             MXFP8 along f (or round it to fp16 for a Q2_K down projection).
+//   down    : the pair covers 256 output rows; the epilogue multiplies by the
+//             routing weight and red-adds into out[t].
+//
+// Warp roles per CTA (persistent, one CTA per SM): warp 0 issues the TMA
+// loads of both operands and, every fourth stage, of the scale factors of the
+// next four stages; warp 1 allocates tensor memory and, in the leader, issues
+// the MMAs; warps 2..9 drain the accumulators.  All loads are TMA (async
+// proxy), so the tensor core reads them with no proxy fence, and both CTAs'
+// loads complete on the leader's barrier.  The accumulator is double-buffered,
+// so a chunk's epilogue overlaps the next chunk's main loop.  Every wait is bounded; a wait that runs out records
+// DS4MOE_ERR_DEVICE_TIMEOUT in the layer's status word and the CTA winds down.
+#include "gemm.cuh"
+
+namespace ds4moe {
+namespace {
+
+enum class PMode { GateUp, Down };
+
+constexpr int kPStages = 7;
+constexpr int kPNMax = 192;     // token columns (N) per chunk, both CTAs together
+constexpr int kPEpiWarps = 8;   // two per tensor-memory lane quarter
+constexpr int kPThreads = 64 + 32 * kPEpiWarps;
+constexpr int kPAcc1 = 192;     // column of the second accumulator buffer
+constexpr int kPSfBase = 384;   // scale-factor slots: SFA 4 + SFB 8 columns each
+constexpr int kPSfSlot = 12;
+constexpr int kPSfSlots = 8;
+constexpr int kSfGroup = 4;     // K blocks whose scale factors one pair of TMA loads brings
+constexpr int kSfRing = 3;      // scale-factor groups in shared memory
+static_assert(kPSfSlots >= kPStages, "scale slots");
+static_assert(kPAcc1 + kPNMax <= kPSfBase && kPSfBase + kPSfSlots * kPSfSlot <= 512, "tensor memory");
+
+struct PSmem {
+  static constexpr int kA = 128 * 128;           // 128 weight rows x 128 K (E2M1 in 8-bit containers)
+  static constexpr int kB = (kPNMax / 2) * 128;  // this CTA's half of the token rows
+  static constexpr int kStage = kA + kB;
+  // scale-factor group: SFA chunks of 4 K blocks (4 x 512) | SFB [4 K blocks][2 row blocks][512]
+  static constexpr int kSfA = kSfGroup * kSfChunk;
+  static constexpr int kSfGroupBytes = kSfA + kSfGroup * 2 * kSfChunk;
+  static constexpr int kSfOff = kPStages * kStage;
+  static constexpr int kXchg = kSfOff + kSfRing * kSfGroupBytes;  // gate/up: silu(g), 4 warp pairs x 16 x 32
+  static constexpr int kColOff = kXchg + 4 * 16 * 32 * 4;      // down: per-column token and weight
+  static constexpr int kBarOff = kColOff + kPNMax * 8;
+  static constexpr int kTotal = kBarOff + 512 + 1024;          // + barriers, + alignment slack
+};
+static_assert(PSmem::kStage % 1024 == 0, "stage alignment");
+static_assert(PSmem::kTotal <= 227 * 1024, "shared memory");
+
+struct PairArgs {
+  int rows_per_expert;  // gate/up: f; down: d
+  int r128;             // 128-row blocks of the activation buffers
+  int K;                // d (gate/up) or f (down)
+  const int32_t* counts;
+  const int32_t* touched;
+  const int32_t* pad_offsets;
+  const int32_t* pad_pair;
+  const float* topk_w;
+  int E, k, d, f;
+  uint8_t* hq;    // gate/up: MXFP8 h codes [rows][f]
+  uint8_t* hsf;   // gate/up: h scales (chunk layout)
+  __half* h16;    // gate/up: fp16 h for a Q2_K down projection, or nullptr
+  float* out;     // down: [T][d]
+  DeviceStatus* status;
+  uint64_t budget_ns;
+  int debug_fault;
+  int split;      // token columns per routed pair: 1, or 2 (hi + lo rows)
+};
+
+// Work sequence shared by every role of both CTAs of a pair: units
+// (touched expert, block pair), expert-major, strided over the pairs; each
+// unit's token columns split into chunks that start on a 128-column boundary
+// (one chunk when they fit in kPNMax).
+struct PairIter {
+  int u, nunits, stride, per_e;
+  int e, pb, ne, t0, nch;
+  const int32_t* counts;
+  const int32_t* touched;
+  int split;
+  __device__ bool first_chunk() {
+    for (; u < nunits; u += stride) {
+      e = __ldg(touched + u / per_e);
+      pb = u % per_e;
+      ne = __ldg(counts + e) * split;
+      if (ne > 0) {
+        t0 = 0;
+        nch = ne <= kPNMax ? ne : 128;
+        return true;
+      }
+    }
+    return false;
+  }
+  __device__ bool next() {
+    t0 += nch;
+    if (t0 < ne) {
+      const int rem = ne - t0;
+      nch = rem <= kPNMax ? rem : 128;
+      return true;
+    }
+    u += stride;
+    return first_chunk();
+  }
+};
+
+// This CTA's 128-row weight tile of a unit.  Gate/up tiles are [E][f/64]
+// (64 gate rows then the same 64 up rows); down tiles are [E][d/128], and the
+// peer's tile of the last pair is past the expert when d is an odd multiple of
+// 128 (its loads then read zeros or the next expert's rows and scales, which
+// are never stored).
+template <PMode M>
+__device__ __forceinline__ int weight_tile(const PairArgs& a, int e, int pb, uint32_t rank) {
+  if (M == PMode::GateUp) return e * (a.f / 64) + 2 * pb + (int)rank;
+  return e * (a.d / 128) + 2 * pb + (int)rank;
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
+template <PMode M>
+__global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                                                               const __grid_constant__ CUtensorMap tm_sfa,
+                                                               const __grid_constant__ CUtensorMap tm_sfb,
+                                                               const __grid_constant__ BoxMaps bmaps,
+                                                               const PairArgs args) {
+  using S = PSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xchg = reinterpret_cast<float*>(smem + S::kXchg);
+  int32_t* col_tok = reinterpret_cast<int32_t*>(smem + S::kColOff);
+  float* col_w = reinterpret_cast<float*>(col_tok + kPNMax);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);  // leader: all bytes of a stage landed
+  uint64_t* empty = full + kPStages;                                  // the stage's MMAs are done
+  uint64_t* acc_full = empty + kPStages;                              // [2] accumulator ready
+  uint64_t* acc_empty = acc_full + 2;                                 // [2] leader: both epilogues drained it
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_ok = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int per_e = M == PMode::GateUp ? args.rows_per_expert / 128 : (args.rows_per_expert + 255) / 256;
+  const int KB = args.K / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&full[s], 1);  // the leader's expect_tx; both CTAs' copies count their bytes
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * kPEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_sfa);
+    prefetch_tmap(&tm_sfb);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrive or copy
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the routing tables and activations of this forward are complete from here on
+  pdl_launch_dependents();
+  const int nunits = __ldg(args.touched + args.E) * per_e;
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool fault_pending = args.debug_fault && blockIdx.x == 0;
+      bool ok = true;
+      int sfg = 0;  // scale-factor groups issued
+      // A group's ring slot is reused three groups later; its last stage must
+      // have been consumed by then.  Full groups (4 stages) are always far
+      // enough back; a chunk with fewer K blocks makes short groups, and then
+      // the producer waits for that stage explicitly.  last0/1/2: the last
+      // stage position of the current group and of the two before it.
+      int pos = 0, last0 = -100, last1 = -100, last2 = -100;
+      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
+        const int nh = round32(it.nch) / 2;  // token rows per CTA
+        const CUtensorMap* tb = &bmaps.m[nh / 16 - 1];
+        const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+        const int brow = prow + (int)rank * nh;
+        const int tile = weight_tile<M>(args, it.e, it.pb, rank);
+        // 4-bit unpacking loads count their packed global bytes
+        const uint32_t bytes = 2u * (128u * 64u + (uint32_t)nh * 128u);
+        constexpr uint32_t kSfBytes = 2u * S::kSfGroupBytes;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
+            report_timeout(args.status, kWhereProducerEmpty);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * S::kStage;
+          const bool sf_load = kb % kSfGroup == 0;  // scale factors of K blocks kb .. kb + 3 (zeros past K)
+          if (sf_load) {
+            const int q = last2;  // last stage of the group whose ring slot this one takes
+            if (q > pos - kPStages &&
+                !mbar_wait_bounded(&empty[q % kPStages], (uint32_t)(q / kPStages) & 1u, args.budget_ns, abort_flag)) {
+              report_timeout(args.status, kWhereProducerEmpty);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            last2 = last1;
+            last1 = last0;
+          }
+          last0 = pos++;
+          if (leader) mbar_arrive_expect_tx(&full[stage], bytes + (sf_load ? kSfBytes : 0u));
+          const uint32_t bar = full0 + 8u * stage;
+          if (fault_pending) {
+            fault_pending = false;  // test-only: drop this stage's operand loads
+          } else {
+            tma_load_2d_pair(st + S::kA, tb, bar, kb * 128, brow);
+            tma_load_2d_pair(st, &tm_a, bar, kb * 128, tile * 128);
+          }
+          if (sf_load) {
+            uint8_t* sf = smem + S::kSfOff + (sfg % kSfRing) * S::kSfGroupBytes;
+            ++sfg;
+            tma_load_2d_pair(sf, &tm_sfa, bar, 0, (tile * KB + kb) * 2);
+            tma_load_3d_pair(sf + S::kSfA, &tm_sfb, bar, 0, (prow / 128) * 2, kb);
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag && leader) {
+        // every issued stage's copies land before the pair exits
+        for (int s = 0; s < kPStages; ++s)
+          if ((issued_mask >> s) & 1u) {
+            volatile int never = 0;
+            mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, args.budget_ns, &never);
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer (leader)
+      PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      uint32_t sf_seq = 0;
+      int sfg = -1;  // scale-factor group in use
+      int chunk = 0;
+      bool ok = true;
+      // Descriptors of stage slot 0 and scale group 0; a slot adds its byte
+      // offset / 16 to the start-address field, a K step of 32 elements adds
+      // 32 bytes.
+      const uint32_t st0 = smem_u32(smem);
+      const uint64_t adesc0 = smem_desc(st0, 16, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(st0 + S::kA, 16, 1024, 2);
+      const uint64_t sfdesc0 = smem_desc(st0 + S::kSfOff, 0, 128, 0);
+      static_assert(S::kXchg < (1 << 18), "descriptor address field");
+      constexpr uint32_t kSfIdStep = (1u << 4) | (1u << 29);  // next byte of the 32-bit scale word, A and B
+      for (bool more = it.first_chunk(); more && ok; more = it.next(), ++chunk) {
+        const int N = round32(it.nch);
+        const int nsf = N > 128 ? 2 : 1;
+        const int buf = chunk & 1;
+        const uint32_t acc = tmem + (uint32_t)(buf ? kPAcc1 : 0);
+        const uint32_t idesc0 = idesc_mx(256, N, 0);
+        if (!mbar_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
+          report_timeout(args.status, kWhereMmaAccEmpty);
+          *abort_flag = 1;
+          break;
+        }
+        acc_phase ^= 1u << buf;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag)) {
+            report_timeout(args.status, kWhereMmaFull);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (kb % kSfGroup == 0) ++sfg;
+          const int j = kb % kSfGroup;
+          const uint64_t soff = (uint64_t)(stage * (S::kStage >> 4));
+          const uint32_t slot = tmem + kPSfBase + (sf_seq++ % kPSfSlots) * kPSfSlot;
+          const uint64_t sd = sfdesc0 + (uint64_t)(((sfg % kSfRing) * S::kSfGroupBytes) >> 4);
+          tc_cp_32x128b_warpx4_pair(slot, sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
+          for (int i = 0; i < nsf; ++i)  // SFB: all token columns (both CTAs hold them)
+            tc_cp_32x128b_warpx4_pair(slot + 4 + 4 * i,
+                                      sd + (uint64_t)((S::kSfA + (2 * j + i) * kSfChunk) >> 4));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)  // K = 32 (32 bytes) per instruction
+            mma_mxf8f6f4_pair(acc, adesc0 + soff + 2 * j, bdesc0 + soff + 2 * j, idesc0 + (uint32_t)j * kSfIdStep,
+                              slot, slot + 4, (kb > 0 || j > 0) ? 1u : 0u);
+          tc_commit_pair(&empty[stage], 0x3);
+          if (++stage == kPStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(&acc_full[buf], 0x3);
+      }
+      // every MMA issued lands before tensor memory is freed
+      tc_commit_pair(drain, 0x1);
+      volatile int never = 0;
+      mbar_wait_bounded(drain, 0, args.budget_ns, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;            // tensor-memory lane quarter this warp may access
+    const int part = (warp - 2) >> 2;  // which half of the 16-column slices
+    const int etid = threadIdx.x - 64;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
+    uint32_t acc_phase = 0;
+    int chunk = 0;
+    for (bool more = it.first_chunk(); more; more = it.next(), ++chunk) {
+      const int N = round32(it.nch);
+      const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+      const int buf = chunk & 1;
+      // One thread takes the accumulator wait and publishes the outcome, so all
+      // epilogue warps leave together (the named barriers need every one).
+      named_bar_sync(1, 32 * kPEpiWarps);  // previous chunk's column table no longer read
+      if (M == PMode::Down) {
+        for (int c = etid; c < it.nch; c += 32 * kPEpiWarps) {
+          const int pr = __ldg(args.pad_pair + prow + c);
+          col_tok[c] = pr / args.k;
+          col_w[c] = __ldg(args.topk_w + pr);
+        }
+      }
+      if (etid == 0) {
+        const bool ok = mbar_wait_bounded(&acc_full[buf], (acc_phase >> buf) & 1u, args.budget_ns, abort_flag);
+        *epi_ok = ok ? 1 : 0;
+        if (!ok) {
+          report_timeout(args.status, kWhereEpiAccFull);
+          *abort_flag = 1;
+        }
+      }
+      named_bar_sync(1, 32 * kPEpiWarps);
+      if (!*epi_ok) break;
+      acc_phase ^= 1u << buf;
+      tc_fence_after();
+      const uint32_t acc = tmem + (uint32_t)(buf ? kPAcc1 : 0) + lane_base;
+      if constexpr (M == PMode::Down) {
+        const int row = (2 * it.pb + (int)rank) * 128 + q * 32 + lane;  // output feature
+        const bool rv = row < args.d;
+        for (int c0 = part * 16; c0 < N; c0 += 32) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(acc + (uint32_t)c0, r);
+          tmem_ld_wait();
+          if (args.split == 2) {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int col = c0 + 2 * jj;
+              if (rv && col < it.nch)
+                red_add_f32(args.out + (size_t)col_tok[col] * args.d + row,
+                            col_w[col] * (__uint_as_float(r[2 * jj]) + __uint_as_float(r[2 * jj + 1])));
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = c0 + jj;
+              if (rv && col < it.nch)
+                red_add_f32(args.out + (size_t)col_tok[col] * args.d + row, col_w[col] * __uint_as_float(r[jj]));
+            }
+          }
+        }
+      } else {
+        // lanes 0..63: gate rows, 64..127: up rows of the same 64 features
+        const bool gate = q < 2;
+        const int pid = part * 2 + (q & 1);  // the gate warp and up warp of one feature quarter
+        float* stg = xchg + pid * (16 * 32);
+        const int i = it.pb * 128 + (int)rank * 64 + (q & 1) * 32 + lane;  // feature in [0, f)
+        for (int c0 = part * 16; c0 < N; c0 += 32) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(acc + (uint32_t)c0, r);
+          tmem_ld_wait();
+          if (gate) {
+            if (args.split == 2) {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj)
+                stg[jj * 32 + lane] = silu(__uint_as_float(r[2 * jj]) + __uint_as_float(r[2 * jj + 1]));
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) stg[jj * 32 + lane] = silu(__uint_as_float(r[jj]));
+            }
+            named_bar_sync(2 + pid, 64);  // staged
+            named_bar_sync(6 + pid, 64);  // taken by the up warp
+            continue;
+          }
+          float sg[16];
+          named_bar_sync(2 + pid, 64);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sg[jj] = stg[jj * 32 + lane];
+          named_bar_sync(6 + pid, 64);
+          if (args.split == 2) {
+            // column pairs (hi, lo) of 8 tokens: add them, then h -> hi + lo rows again
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float u = __uint_as_float(r[2 * jj]) + __uint_as_float(r[2 * jj + 1]);
+              const float h = sg[jj] * u;
+              const float a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+              const int s = mxfp8_exponent(a);
+              const uint32_t chi = f32x2_to_e4m3x2(h * exp2i(-s), 0.f) & 0xFFu;
+              const float res = h - e4m3x2_to_f32x2(chi).x * exp2i(s);
+              const float a2 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(res))));
+              const int s2 = mxfp8_exponent(a2);
+              const uint32_t clo = f32x2_to_e4m3x2(res * exp2i(-s2), 0.f) & 0xFFu;
+              const int col = c0 + 2 * jj;
+              if (col < it.nch) {
+                const size_t row = (size_t)(prow + col);
+                args.hq[row * args.f + i] = (uint8_t)chi;
+                args.hq[(row + 1) * args.f + i] = (uint8_t)clo;
+                if (lane == 0) {
+                  args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
+                  args.hsf[act_sf_index(row + 1, i / 32, args.r128)] = (uint8_t)(s2 + 127);
+                }
+              }
+            }
+            continue;
+          }
+          float h[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) h[jj] = sg[jj] * __uint_as_float(r[jj]);
+          if (args.h16 != nullptr) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (c0 + jj < it.nch) args.h16[(size_t)(prow + c0 + jj) * args.f + i] = __float2half_rn(h[jj]);
+          } else {
+            uint32_t amax[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) amax[jj] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj])));
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = c0 + jj;
+              if (col < it.nch) {
+                const int s = mxfp8_exponent(__uint_as_float(amax[jj]));
+                const size_t row = (size_t)(prow + col);
+                args.hq[row * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
+                if (lane == 0) args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&acc_empty[buf]);
+        else mbar_arrive_cluster(acc_empty0 + 8u * buf);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's accumulator reads and the leader's MMAs are done in both CTAs
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+// Largest number of resident pairs of a kernel (clusters of two CTAs with
+// this shared memory), asked once.
+template <PMode M>
+int max_pairs(int num_sms) {
+  static int cached = 0;
+  if (cached > 0) return cached;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = PSmem::kTotal;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)pair_gemm_kernel<M>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  cached = n;
+  return n;
+}
+
+template <PMode M>
+cudaError_t launch_pair(const ds4moe_layer* L, const CUtensorMap& a, const CUtensorMap& sfa, const CUtensorMap& sfb,
+                        const CUtensorMap* b, const PairArgs& args, cudaStream_t st) {
+  BoxMaps maps;
+  for (int i = 0; i < kNumBoxMaps; ++i) maps.m[i] = b[i];
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute((const void*)pair_gemm_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PSmem::kTotal);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int per_e = M == PMode::GateUp ? args.rows_per_expert / 128 : (args.rows_per_expert + 255) / 256;
+  const int units = args.E * per_e;
+  const int mp = max_pairs<M>(L->num_sms);
+  const int pairs = units < mp ? units : mp;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = PSmem::kTotal;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<M>, a, sfa, sfb, maps, args);
+}
+
+PairArgs pair_args(const ds4moe_layer* L, int split) {
+  PairArgs a{};
+  a.counts = L->s.counts;
+  a.touched = L->s.touched;
+  a.pad_offsets = L->s.pad_offsets;
+  a.pad_pair = L->s.pad_pair;
+  a.topk_w = L->s.topk_w;
+  a.E = L->cfg.n_experts;
+  a.k = L->cfg.top_k;
+  a.d = L->cfg.d_model;
+  a.f = L->cfg.d_ff;
+  a.status = L->status;
+  a.r128 = (int)(L->s.pad_rows_max / 128);
+  a.debug_fault = L->cfg.debug_fault;
+  a.split = split;
+  a.budget_ns = L->cfg.debug_fault ? 1000000ull : (uint64_t)L->cfg.wait_timeout_ms * 1000000ull;
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStream_t st) {
+  (void)T;
+  PairArgs a = pair_args(L, split);
+  a.rows_per_expert = L->cfg.d_ff;
+  a.K = L->cfg.d_model;
+  a.hq = L->s.hq;
+  a.hsf = L->s.hsf;
+  a.h16 = (L->cfg.down_format == DS4MOE_DOWN_Q2K) ? L->s.h16 : nullptr;
+  return launch_pair<PMode::GateUp>(L, L->tm_gu, L->tm_sfa_gu, L->tm_sfb_x, L->tm_xq, a, st);
+}
+
+cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st) {
+  (void)T;
+  PairArgs a = pair_args(L, split);
+  a.debug_fault = 0;
+  a.rows_per_expert = L->cfg.d_model;
+  a.K = L->cfg.d_ff;
+  a.out = out;
+  return launch_pair<PMode::Down>(L, L->tm_down, L->tm_sfa_dn, L->tm_sfb_h, L->tm_hq, a, st);
+}
+
+}  // namespace ds4moe

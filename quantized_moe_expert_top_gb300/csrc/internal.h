@@ -96,8 +96,12 @@ struct ds4moe_layer {
   ds4moe::Scratch s;
   ds4moe::DeviceStatus* status;  // device
   // TMA descriptors (64-byte aligned inside the struct)
-  CUtensorMap tm_gu;     // 4-bit gate+up weights, box 128 x 256 rows
+  CUtensorMap tm_gu;     // 4-bit gate+up weights, box 128 x 128 rows (64 gate + 64 up)
   CUtensorMap tm_down;   // 4-bit down weights, box 128 x 128 rows
+  CUtensorMap tm_sfa_gu;  // gate/up weight scale chunks, 4 consecutive K blocks per box
+  CUtensorMap tm_sfa_dn;  // down weight scale chunks, same
+  CUtensorMap tm_sfb_x;   // x scale chunks: 2 row blocks x 4 K blocks per box
+  CUtensorMap tm_sfb_h;   // h scale chunks, same
   CUtensorMap tm_xq[ds4moe::kNumBoxMaps];   // 8-bit x, boxes 128 B x (16 * (i + 1)) rows
   CUtensorMap tm_hq[ds4moe::kNumBoxMaps];   // 8-bit h
   CUtensorMap tm_h16[ds4moe::kNumBoxMaps];  // fp16 h, boxes 64 x (16 * (i + 1)) rows
@@ -131,8 +135,8 @@ cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
 
 // create-time repacking
-cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int chunk_stride,
-                             int chunk_off, cudaStream_t st);
+cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int tile_rows, int row_off,
+                             cudaStream_t st);
 cudaError_t launch_pack_gu(const ds4moe_weights* w, ds4moe_layer* L, cudaStream_t st);
 cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream_t st);
 cudaError_t launch_pack_rows(uint8_t* dst, int pitch, int64_t rows, const uint8_t* s0, int l0, const uint8_t* s1,

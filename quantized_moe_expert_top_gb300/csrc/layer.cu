@@ -15,38 +15,38 @@ using namespace ds4moe;
 namespace {
 
 // Scale bytes [E][rows][K/32] (one per 32-element block) -> the chunk layout the
-// tensor-core scale copy reads: per (expert, 128-row block, 128-K block) one
-// 512-byte chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kblock % 4) for row r of
-// the block.
-// (Chunk c of the output starts at c * chunk_stride + chunk_off bytes, so two
-// matrices' chunks can be interleaved.)
+// tensor-core scale copy reads: one 512-byte chunk per (weight tile, 128-K
+// block), byte (t % 32) * 16 + (t / 32) * 4 + (kblock % 4) for tile row t.
+// A tile takes `tile_rows` consecutive rows of the matrix (128, or 64 when the
+// gate and up rows of 64 features share a tile) at tile rows row_off.. .
 __global__ void repack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int rows, int K,
-                                 int chunk_stride, int chunk_off) {
+                                 int tile_rows, int row_off) {
   const int nkb = K / 32;
   const size_t total = (size_t)E * rows * nkb;
-  const int MB = rows / kBM, KB = K / kBK;
+  const int tiles_per_e = rows / tile_rows, KB = K / kBK;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int kb = (int)(i % nkb);
     const size_t er = i / nkb;
     const int r = (int)(er % rows);
     const int e = (int)(er / rows);
-    const size_t chunk = ((size_t)e * MB + r / kBM) * KB + kb / 4;
-    const int rr = r % kBM;
-    dst[chunk * chunk_stride + chunk_off + (rr % 32) * 16 + (rr / 32) * 4 + (kb % 4)] = src[i];
+    const size_t chunk = ((size_t)e * tiles_per_e + r / tile_rows) * KB + kb / 4;
+    const int t = r % tile_rows + row_off;
+    dst[chunk * kSfChunk + (t % 32) * 16 + (t / 32) * 4 + (kb % 4)] = src[i];
   }
 }
 
-// Gate/up rows into the tile-major layout: for expert e and 128-row block mb,
-// 128 gate rows then the same 128 up rows, each codes | scales | padding.
+// Gate/up rows into the tile-major layout: for expert e and 64-feature block
+// fb, the 64 gate rows then the same 64 up rows (one 128-row weight tile of
+// the paired GEMM), each codes | scales | padding.
 __global__ void pack_gu_kernel(uint8_t* __restrict__ dst, int pitch, int E, int d, int f,
                                const uint8_t* __restrict__ gc, const uint8_t* __restrict__ gs,
                                const uint8_t* __restrict__ uc, const uint8_t* __restrict__ us) {
   const int64_t rows = (int64_t)E * f * 2;
   for (int64_t R = blockIdx.x; R < rows; R += gridDim.x) {
     const int r = (int)(R % 128);
-    const int j = (int)((R / 128) % 2);
-    const int64_t eb = R / 256;  // e * (f/128) + mb
-    const int64_t src_row = eb * 128 + r;  // = e * f + mb * 128 + r
+    const int j = r / 64;
+    const int64_t t = R / 128;                 // e * (f/64) + fb
+    const int64_t src_row = t * 64 + r % 64;   // = e * f + fb * 64 + r % 64
     const uint32_t* c = reinterpret_cast<const uint32_t*>((j ? uc : gc) + src_row * (d / 2));
     const uint32_t* sc = reinterpret_cast<const uint32_t*>((j ? us : gs) + src_row * (d / 32));
     uint32_t* o = reinterpret_cast<uint32_t*>(dst + R * pitch);
@@ -126,6 +126,34 @@ bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, void* base, uint64_t inn
   cuuint32_t estr[2] = {1, 1};
   return fn(tm, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Scale-factor chunk arrays as rows of 256 bytes (two rows per 512-byte
+// chunk), no swizzle.  Weight scales [tiles][K/128][512]: 2-D, box 256 x 8 =
+// the chunks of 4 consecutive K blocks of one tile.  Activation scales
+// [K/128][rows/128][512]: 3-D {256, 2 * rows/128, K/128}, box 256 x 4 x 4 =
+// 2 row blocks x 4 K blocks.
+bool encode_sf_weights(CUtensorMap* tm, void* base, uint64_t chunks) {
+  PFN_encodeTiled fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {256, chunks * 2};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 8};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool encode_sf_acts(CUtensorMap* tm, void* base, uint64_t r128, uint64_t kblocks) {
+  PFN_encodeTiled fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {256, r128 * 2, kblocks};
+  cuuint64_t strides[2] = {256, r128 * 512};
+  cuuint32_t box[3] = {256, 4, 4};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -319,9 +347,9 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       goto fail;
     }
     if (need_pre) {
-      if (launch_repack_sf(wts->gate_scales, w.gu_sf, E, f, d, 2 * kSfChunk, 0, st) != cudaSuccess ||
-          launch_repack_sf(wts->up_scales, w.gu_sf, E, f, d, 2 * kSfChunk, kSfChunk, st) != cudaSuccess ||
-          (!q2k && launch_repack_sf(wts->down_scales, w.down_sf, E, d, f, kSfChunk, 0, st) != cudaSuccess)) {
+      if (launch_repack_sf(wts->gate_scales, w.gu_sf, E, f, d, 64, 0, st) != cudaSuccess ||
+          launch_repack_sf(wts->up_scales, w.gu_sf, E, f, d, 64, 64, st) != cudaSuccess ||
+          (!q2k && launch_repack_sf(wts->down_scales, w.down_sf, E, d, f, 128, 0, st) != cudaSuccess)) {
         rc = DS4MOE_ERR_CUDA;
         goto fail;
       }
@@ -332,7 +360,7 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
     }
     if (need_pre) {
       bool tm_ok = encode_2d(&L->tm_gu, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu, d, (uint64_t)E * f * 2,
-                             w.pitch_gu, 128, 256);
+                             w.pitch_gu, 128, 128);
       for (int b = 0; b < kNumBoxMaps; ++b) {
         const uint32_t rows = 16u * (uint32_t)(b + 1);
         tm_ok = tm_ok && encode_2d(&L->tm_xq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, d, pad_rows, d, 128, rows);
@@ -345,6 +373,13 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       if (!q2k)
         tm_ok = tm_ok && encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn, f, (uint64_t)E * d,
                                    w.pitch_dn, 128, 128);
+      const uint64_t r128 = (uint64_t)pad_rows / 128;
+      tm_ok = tm_ok && encode_sf_weights(&L->tm_sfa_gu, w.gu_sf, (uint64_t)E * (f / 64) * (d / 128));
+      tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_x, s.xsf, r128, (uint64_t)d / 128);
+      if (!q2k) {
+        tm_ok = tm_ok && encode_sf_weights(&L->tm_sfa_dn, w.down_sf, (uint64_t)E * (d / 128) * (f / 128));
+        tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h, s.hsf, r128, (uint64_t)f / 128);
+      }
       if (!tm_ok) {
         rc = DS4MOE_ERR_CUDA;
         goto fail;
@@ -539,11 +574,11 @@ void ds4moe_destroy(ds4moe_layer* L) {
 
 namespace ds4moe {
 
-cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int chunk_stride,
-                             int chunk_off, cudaStream_t st) {
+cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int tile_rows, int row_off,
+                             cudaStream_t st) {
   const size_t total = (size_t)E * rows * (K / 32);
   const int blocks = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
-  repack_sf_kernel<<<blocks, 256, 0, st>>>(scales, sf, E, rows, K, chunk_stride, chunk_off);
+  repack_sf_kernel<<<blocks, 256, 0, st>>>(scales, sf, E, rows, K, tile_rows, row_off);
   return cudaGetLastError();
 }
 
