@@ -46,7 +46,7 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
 }
 
 // Token-tile tensor maps, one per box height 16, 32, ..., 192 rows.
-struct alignas(64) BoxMaps {
+struct alignas(128) BoxMaps {
   CUtensorMap m[kNumBoxMaps];
 };
 

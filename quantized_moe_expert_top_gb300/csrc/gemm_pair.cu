@@ -39,18 +39,22 @@ namespace {
 
 enum class PMode { GateUp, Down };
 
-constexpr int kPStages = 7;
+constexpr int kPStages = 6;     // K = 128 stage slots, loaded and consumed two at a time
+constexpr int kPBars = kPStages / 2;
 constexpr int kPNMax = 192;     // token columns (N) per chunk, both CTAs together
 constexpr int kPEpiWarps = 8;   // two per tensor-memory lane quarter
-constexpr int kPThreads = 64 + 32 * kPEpiWarps;
+constexpr int kPThreads = 32 * (2 + kPEpiWarps);
 constexpr int kPAcc1 = 192;     // column of the second accumulator buffer
 constexpr int kPSfBase = 384;   // scale-factor slots: SFA 4 + SFB 8 columns each
 constexpr int kPSfSlot = 12;
-constexpr int kPSfSlots = 8;
+// Scale-factor slots in tensor memory, one per stage in issue order.  A slot
+// is rewritten (tcgen05.cp) only once the MMAs that read it are known to be
+// complete: the stages kPStages back are done before new ones are loaded.
+constexpr int kPSfSlots = kPStages + 1;
+static_assert(kPAcc1 + kPNMax <= kPSfBase && kPSfBase + kPSfSlots * kPSfSlot <= 512, "tensor memory");
 constexpr int kSfGroup = 4;     // K blocks whose scale factors one pair of TMA loads brings
 constexpr int kSfRing = 3;      // scale-factor groups in shared memory
-static_assert(kPSfSlots >= kPStages, "scale slots");
-static_assert(kPAcc1 + kPNMax <= kPSfBase && kPSfBase + kPSfSlots * kPSfSlot <= 512, "tensor memory");
+static_assert(kSfGroup % 2 == 0, "scale groups start on a step boundary");
 
 struct PSmem {
   static constexpr int kA = 128 * 128;           // 128 weight rows x 128 K (E2M1 in 8-bit containers)
@@ -60,8 +64,8 @@ struct PSmem {
   static constexpr int kSfA = kSfGroup * kSfChunk;
   static constexpr int kSfGroupBytes = kSfA + kSfGroup * 2 * kSfChunk;
   static constexpr int kSfOff = kPStages * kStage;
-  static constexpr int kXchg = kSfOff + kSfRing * kSfGroupBytes;  // gate/up: silu(g), 4 warp pairs x 16 x 32
-  static constexpr int kColOff = kXchg + 4 * 16 * 32 * 4;      // down: per-column token and weight
+  static constexpr int kXchg = kSfOff + kSfRing * kSfGroupBytes;  // gate/up: 4 warp pairs x (silu(g), u) x 8 x 32
+  static constexpr int kColOff = kXchg + 4 * 2 * 8 * 32 * 4;   // down: per-column token and weight
   static constexpr int kBarOff = kColOff + kPNMax * 8;
   static constexpr int kTotal = kBarOff + 512 + 1024;          // + barriers, + alignment slack
 };
@@ -136,6 +140,81 @@ __device__ __forceinline__ int weight_tile(const PairArgs& a, int e, int pb, uin
 
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
+// One 16-column slice of the gate/up epilogue for a warp pair (the gate warp
+// and the up warp of one feature quarter; lane = feature): each warp stages
+// the half of its per-token values that the other warp finishes, then forms
+// h = silu(g) * u for its own half of the tokens and stores h in MXFP8 (32
+// features = one scale block = the warp's lanes), as hi + lo rows for the
+// split activations, or in fp16 for a Q2_K down projection.  SPLIT columns
+// make one token.
+template <int SPLIT>
+__device__ __forceinline__ void gateup_slice(const uint32_t (&r)[16], bool gate, int lane, float* sg, float* su,
+                                             int pid, int c0, int nch, int prow, int i, const PairArgs& args) {
+  constexpr int kTok = 16 / SPLIT;  // tokens in the slice
+  constexpr int kHalf = kTok / 2;   // tokens each warp finishes
+  float v[kTok];
+#pragma unroll
+  for (int jj = 0; jj < kTok; ++jj)
+    v[jj] = SPLIT == 2 ? __uint_as_float(r[2 * jj]) + __uint_as_float(r[2 * jj + 1]) : __uint_as_float(r[jj]);
+  if (gate) {
+#pragma unroll
+    for (int jj = 0; jj < kTok; ++jj) v[jj] = silu(v[jj]);
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) sg[jj * 32 + lane] = v[kHalf + jj];
+  } else {
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) su[jj * 32 + lane] = v[jj];
+  }
+  named_bar_sync(2 + pid, 64);  // both halves staged
+  float h[kHalf];
+#pragma unroll
+  for (int jj = 0; jj < kHalf; ++jj) h[jj] = gate ? v[jj] * su[jj * 32 + lane] : sg[jj * 32 + lane] * v[kHalf + jj];
+  named_bar_sync(6 + pid, 64);  // staging free for the next slice
+  const int tok0 = c0 / SPLIT + (gate ? 0 : kHalf);  // first token of this warp's half
+  if constexpr (SPLIT == 2) {
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) {
+      const float a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj]))));
+      const int s = mxfp8_exponent(a);
+      const uint32_t chi = f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu;
+      const float res = h[jj] - e4m3x2_to_f32x2(chi).x * exp2i(s);
+      const float a2 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(res))));
+      const int s2 = mxfp8_exponent(a2);
+      const uint32_t clo = f32x2_to_e4m3x2(res * exp2i(-s2), 0.f) & 0xFFu;
+      const int col = 2 * (tok0 + jj);
+      if (col < nch) {
+        const size_t row = (size_t)(prow + col);
+        args.hq[row * args.f + i] = (uint8_t)chi;
+        args.hq[(row + 1) * args.f + i] = (uint8_t)clo;
+        if (lane == 0) {
+          args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
+          args.hsf[act_sf_index(row + 1, i / 32, args.r128)] = (uint8_t)(s2 + 127);
+        }
+      }
+    }
+  } else {
+    if (args.h16 != nullptr) {
+#pragma unroll
+      for (int jj = 0; jj < kHalf; ++jj)
+        if (tok0 + jj < nch) args.h16[(size_t)(prow + tok0 + jj) * args.f + i] = __float2half_rn(h[jj]);
+      return;
+    }
+    uint32_t amax[kHalf];
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) amax[jj] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj])));
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) {
+      const int col = tok0 + jj;
+      if (col < nch) {
+        const int s = mxfp8_exponent(__uint_as_float(amax[jj]));
+        const size_t row = (size_t)(prow + col);
+        args.hq[row * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
+        if (lane == 0) args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
+      }
+    }
+  }
+}
+
 template <PMode M>
 __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                                                                const __grid_constant__ CUtensorMap tm_sfa,
@@ -148,9 +227,9 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
   float* xchg = reinterpret_cast<float*>(smem + S::kXchg);
   int32_t* col_tok = reinterpret_cast<int32_t*>(smem + S::kColOff);
   float* col_w = reinterpret_cast<float*>(col_tok + kPNMax);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);  // leader: all bytes of a stage landed
-  uint64_t* empty = full + kPStages;                                  // the stage's MMAs are done
-  uint64_t* acc_full = empty + kPStages;                              // [2] accumulator ready
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);  // leader: all bytes of a slot pair landed
+  uint64_t* empty = full + kPBars;                                    // the slot pair's MMAs are done
+  uint64_t* acc_full = empty + kPBars;                                // [2] accumulator ready
   uint64_t* acc_empty = acc_full + 2;                                 // [2] leader: both epilogues drained it
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -164,7 +243,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
   const int KB = args.K / 128;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < kPBars; ++s) {
       mbar_init(&full[s], 1);  // the leader's expect_tx; both CTAs' copies count their bytes
       mbar_init(&empty[s], 1);
     }
@@ -195,21 +274,21 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
+    // A step loads two K blocks (one when a chunk has an odd count left) into
+    // one slot pair, completing on one barrier, so the MMA issuer waits once
+    // per eight MMAs.  Every fourth K block (a step boundary) also brings the
+    // scale factors of the next four.  The scale ring slot of a group is
+    // reused three groups later; a group spans at least one step, so its
+    // steps are at least kPBars steps back and done by then.
     if (lane == 0) {
       PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);
-      int stage = 0;
+      int bar = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool fault_pending = args.debug_fault && blockIdx.x == 0;
       bool ok = true;
       int sfg = 0;  // scale-factor groups issued
-      // A group's ring slot is reused three groups later; its last stage must
-      // have been consumed by then.  Full groups (4 stages) are always far
-      // enough back; a chunk with fewer K blocks makes short groups, and then
-      // the producer waits for that stage explicitly.  last0/1/2: the last
-      // stage position of the current group and of the two before it.
-      int pos = 0, last0 = -100, last1 = -100, last2 = -100;
       for (bool more = it.first_chunk(); more && ok; more = it.next()) {
         const int nh = round32(it.nch) / 2;  // token rows per CTA
         const CUtensorMap* tb = &bmaps.m[nh / 16 - 1];
@@ -217,58 +296,48 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         const int brow = prow + (int)rank * nh;
         const int tile = weight_tile<M>(args, it.e, it.pb, rank);
         // 4-bit unpacking loads count their packed global bytes
-        const uint32_t bytes = 2u * (128u * 64u + (uint32_t)nh * 128u);
+        const uint32_t stage_bytes = 2u * (128u * 64u + (uint32_t)nh * 128u);
         constexpr uint32_t kSfBytes = 2u * S::kSfGroupBytes;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
+        for (int kb = 0; kb < KB; kb += 2) {
+          if (!mbar_wait_bounded(&empty[bar], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          uint8_t* st = smem + stage * S::kStage;
+          const int nst = KB - kb >= 2 ? 2 : 1;
           const bool sf_load = kb % kSfGroup == 0;  // scale factors of K blocks kb .. kb + 3 (zeros past K)
-          if (sf_load) {
-            const int q = last2;  // last stage of the group whose ring slot this one takes
-            if (q > pos - kPStages &&
-                !mbar_wait_bounded(&empty[q % kPStages], (uint32_t)(q / kPStages) & 1u, args.budget_ns, abort_flag)) {
-              report_timeout(args.status, kWhereProducerEmpty);
-              *abort_flag = 1;
-              ok = false;
-              break;
+          const uint32_t b_cl = full0 + 8u * bar;
+          if (leader) mbar_arrive_expect_tx(&full[bar], stage_bytes * nst + (sf_load ? kSfBytes : 0u));
+          for (int i = 0; i < nst; ++i) {
+            uint8_t* st = smem + (2 * bar + i) * S::kStage;
+            if (fault_pending) {
+              fault_pending = false;  // test-only: drop this stage's operand loads
+            } else {
+              tma_load_2d_pair(st + S::kA, tb, b_cl, (kb + i) * 128, brow);
+              tma_load_2d_pair(st, &tm_a, b_cl, (kb + i) * 128, tile * 128);
             }
-            last2 = last1;
-            last1 = last0;
-          }
-          last0 = pos++;
-          if (leader) mbar_arrive_expect_tx(&full[stage], bytes + (sf_load ? kSfBytes : 0u));
-          const uint32_t bar = full0 + 8u * stage;
-          if (fault_pending) {
-            fault_pending = false;  // test-only: drop this stage's operand loads
-          } else {
-            tma_load_2d_pair(st + S::kA, tb, bar, kb * 128, brow);
-            tma_load_2d_pair(st, &tm_a, bar, kb * 128, tile * 128);
           }
           if (sf_load) {
             uint8_t* sf = smem + S::kSfOff + (sfg % kSfRing) * S::kSfGroupBytes;
             ++sfg;
-            tma_load_2d_pair(sf, &tm_sfa, bar, 0, (tile * KB + kb) * 2);
-            tma_load_3d_pair(sf + S::kSfA, &tm_sfb, bar, 0, (prow / 128) * 2, kb);
+            tma_load_2d_pair(sf, &tm_sfa, b_cl, 0, (tile * KB + kb) * 2);
+            tma_load_3d_pair(sf + S::kSfA, &tm_sfb, b_cl, 0, (prow / 128) * 2, kb);
           }
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kPStages) {
-            stage = 0;
+          issued_mask |= 1u << bar;
+          issued_parity = (issued_parity & ~(1u << bar)) | (phase << bar);
+          if (++bar == kPBars) {
+            bar = 0;
             phase ^= 1u;
           }
         }
       }
       if (*abort_flag && leader) {
-        // every issued stage's copies land before the pair exits
-        for (int s = 0; s < kPStages; ++s)
-          if ((issued_mask >> s) & 1u) {
+        // every issued step's copies land before the pair exits
+        for (int b = 0; b < kPBars; ++b)
+          if ((issued_mask >> b) & 1u) {
             volatile int never = 0;
-            mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, args.budget_ns, &never);
+            mbar_wait_bounded(&full[b], (issued_parity >> b) & 1u, args.budget_ns, &never);
           }
       }
     }
@@ -277,11 +346,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer (leader)
       PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      uint32_t sf_seq = 0;
-      int sfg = -1;  // scale-factor group in use
-      int chunk = 0;
+      int bar = 0, sfg = -1, chunk = 0;
+      uint32_t phase = 0, acc_phase = 0, sf_seq = 0;
       bool ok = true;
       // Descriptors of stage slot 0 and scale group 0; a slot adds its byte
       // offset / 16 to the start-address field, a K step of 32 elements adds
@@ -305,30 +371,33 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         }
         acc_phase ^= 1u << buf;
         tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag)) {
+        for (int kb = 0; kb < KB; kb += 2) {
+          if (!mbar_wait_bounded(&full[bar], phase, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereMmaFull);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          tc_fence_after();
+          const int nst = KB - kb >= 2 ? 2 : 1;
           if (kb % kSfGroup == 0) ++sfg;
-          const int j = kb % kSfGroup;
-          const uint64_t soff = (uint64_t)(stage * (S::kStage >> 4));
-          const uint32_t slot = tmem + kPSfBase + (sf_seq++ % kPSfSlots) * kPSfSlot;
           const uint64_t sd = sfdesc0 + (uint64_t)(((sfg % kSfRing) * S::kSfGroupBytes) >> 4);
-          tc_cp_32x128b_warpx4_pair(slot, sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
-          for (int i = 0; i < nsf; ++i)  // SFB: all token columns (both CTAs hold them)
-            tc_cp_32x128b_warpx4_pair(slot + 4 + 4 * i,
-                                      sd + (uint64_t)((S::kSfA + (2 * j + i) * kSfChunk) >> 4));
+          for (int i = 0; i < nst; ++i) {
+            const int j = (kb + i) % kSfGroup;
+            const uint64_t soff = (uint64_t)((2 * bar + i) * (S::kStage >> 4));
+            const uint32_t slot = tmem + kPSfBase + (sf_seq % kPSfSlots) * kPSfSlot;
+            sf_seq = sf_seq + 1 == kPSfSlots ? 0 : sf_seq + 1;
+            tc_cp_32x128b_warpx4_pair(slot, sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
+            for (int c = 0; c < nsf; ++c)  // SFB: all token columns (both CTAs hold them)
+              tc_cp_32x128b_warpx4_pair(slot + 4 + 4 * c,
+                                        sd + (uint64_t)((S::kSfA + (2 * j + c) * kSfChunk) >> 4));
 #pragma unroll
-          for (int j = 0; j < 4; ++j)  // K = 32 (32 bytes) per instruction
-            mma_mxf8f6f4_pair(acc, adesc0 + soff + 2 * j, bdesc0 + soff + 2 * j, idesc0 + (uint32_t)j * kSfIdStep,
-                              slot, slot + 4, (kb > 0 || j > 0) ? 1u : 0u);
-          tc_commit_pair(&empty[stage], 0x3);
-          if (++stage == kPStages) {
-            stage = 0;
+            for (int jj = 0; jj < 4; ++jj)  // K = 32 (32 bytes) per instruction
+              mma_mxf8f6f4_pair(acc, adesc0 + soff + 2 * jj, bdesc0 + soff + 2 * jj,
+                                idesc0 + (uint32_t)jj * kSfIdStep, slot, slot + 4, (kb + i > 0 || jj > 0) ? 1u : 0u);
+          }
+          tc_commit_pair(&empty[bar], 0x3);
+          if (++bar == kPBars) {
+            bar = 0;
             phase ^= 1u;
           }
         }
@@ -343,11 +412,19 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;            // tensor-memory lane quarter this warp may access
+    const int q = warp & 3;                         // tensor-memory lane quarter this warp may access
     const int part = (warp - 2) >> 2;  // which half of the 16-column slices
     const int etid = threadIdx.x - 64;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    auto release = [&](int b) {  // the buffer's reads are done: free it for the next chunk
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&acc_empty[b]);
+        else mbar_arrive_cluster(acc_empty0 + 8u * b);
+      }
+    };
     PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
     uint32_t acc_phase = 0;
     int chunk = 0;
@@ -403,89 +480,25 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
           }
         }
       } else {
-        // lanes 0..63: gate rows, 64..127: up rows of the same 64 features
+        // Lanes 0..63 hold gate rows, 64..127 the up rows of the same 64
+        // features.  The gate warp and the up warp of one feature quarter
+        // each finish half of a 16-column slice: the gate warp the first
+        // half (with u from the up warp), the up warp the second half (with
+        // silu(g) from the gate warp).
         const bool gate = q < 2;
-        const int pid = part * 2 + (q & 1);  // the gate warp and up warp of one feature quarter
-        float* stg = xchg + pid * (16 * 32);
+        const int pid = part * 2 + (q & 1);  // the warp pair of one feature quarter
+        float* sg = xchg + pid * (2 * 8 * 32);  // silu(g) of the second half: [8][32]
+        float* su = sg + 8 * 32;                // u of the first half: [8][32]
         const int i = it.pb * 128 + (int)rank * 64 + (q & 1) * 32 + lane;  // feature in [0, f)
         for (int c0 = part * 16; c0 < N; c0 += 32) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(acc + (uint32_t)c0, r);
           tmem_ld_wait();
-          if (gate) {
-            if (args.split == 2) {
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj)
-                stg[jj * 32 + lane] = silu(__uint_as_float(r[2 * jj]) + __uint_as_float(r[2 * jj + 1]));
-            } else {
-#pragma unroll
-              for (int jj = 0; jj < 16; ++jj) stg[jj * 32 + lane] = silu(__uint_as_float(r[jj]));
-            }
-            named_bar_sync(2 + pid, 64);  // staged
-            named_bar_sync(6 + pid, 64);  // taken by the up warp
-            continue;
-          }
-          float sg[16];
-          named_bar_sync(2 + pid, 64);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) sg[jj] = stg[jj * 32 + lane];
-          named_bar_sync(6 + pid, 64);
-          if (args.split == 2) {
-            // column pairs (hi, lo) of 8 tokens: add them, then h -> hi + lo rows again
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const float u = __uint_as_float(r[2 * jj]) + __uint_as_float(r[2 * jj + 1]);
-              const float h = sg[jj] * u;
-              const float a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
-              const int s = mxfp8_exponent(a);
-              const uint32_t chi = f32x2_to_e4m3x2(h * exp2i(-s), 0.f) & 0xFFu;
-              const float res = h - e4m3x2_to_f32x2(chi).x * exp2i(s);
-              const float a2 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(res))));
-              const int s2 = mxfp8_exponent(a2);
-              const uint32_t clo = f32x2_to_e4m3x2(res * exp2i(-s2), 0.f) & 0xFFu;
-              const int col = c0 + 2 * jj;
-              if (col < it.nch) {
-                const size_t row = (size_t)(prow + col);
-                args.hq[row * args.f + i] = (uint8_t)chi;
-                args.hq[(row + 1) * args.f + i] = (uint8_t)clo;
-                if (lane == 0) {
-                  args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
-                  args.hsf[act_sf_index(row + 1, i / 32, args.r128)] = (uint8_t)(s2 + 127);
-                }
-              }
-            }
-            continue;
-          }
-          float h[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) h[jj] = sg[jj] * __uint_as_float(r[jj]);
-          if (args.h16 != nullptr) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              if (c0 + jj < it.nch) args.h16[(size_t)(prow + c0 + jj) * args.f + i] = __float2half_rn(h[jj]);
-          } else {
-            uint32_t amax[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) amax[jj] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj])));
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int col = c0 + jj;
-              if (col < it.nch) {
-                const int s = mxfp8_exponent(__uint_as_float(amax[jj]));
-                const size_t row = (size_t)(prow + col);
-                args.hq[row * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
-                if (lane == 0) args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
-              }
-            }
-          }
+          if (args.split == 2) gateup_slice<2>(r, gate, lane, sg, su, pid, c0, it.nch, prow, i, args);
+          else gateup_slice<1>(r, gate, lane, sg, su, pid, c0, it.nch, prow, i, args);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(&acc_empty[buf]);
-        else mbar_arrive_cluster(acc_empty0 + 8u * buf);
-      }
+      release(buf);
     }
   }
 
