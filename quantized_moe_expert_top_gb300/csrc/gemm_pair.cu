@@ -381,19 +381,25 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
           const int nst = KB - kb >= 2 ? 2 : 1;
           if (kb % kSfGroup == 0) ++sfg;
           const uint64_t sd = sfdesc0 + (uint64_t)(((sfg % kSfRing) * S::kSfGroupBytes) >> 4);
+          // scale factors of both stages first, so the second stage's copies
+          // run while the first stage's MMAs do
+          uint32_t slot[2];
           for (int i = 0; i < nst; ++i) {
             const int j = (kb + i) % kSfGroup;
-            const uint64_t soff = (uint64_t)((2 * bar + i) * (S::kStage >> 4));
-            const uint32_t slot = tmem + kPSfBase + (sf_seq % kPSfSlots) * kPSfSlot;
+            slot[i] = tmem + kPSfBase + sf_seq * kPSfSlot;
             sf_seq = sf_seq + 1 == kPSfSlots ? 0 : sf_seq + 1;
-            tc_cp_32x128b_warpx4_pair(slot, sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
+            tc_cp_32x128b_warpx4_pair(slot[i], sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
             for (int c = 0; c < nsf; ++c)  // SFB: all token columns (both CTAs hold them)
-              tc_cp_32x128b_warpx4_pair(slot + 4 + 4 * c,
+              tc_cp_32x128b_warpx4_pair(slot[i] + 4 + 4 * c,
                                         sd + (uint64_t)((S::kSfA + (2 * j + c) * kSfChunk) >> 4));
+          }
+          for (int i = 0; i < nst; ++i) {
+            const uint64_t soff = (uint64_t)((2 * bar + i) * (S::kStage >> 4));
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)  // K = 32 (32 bytes) per instruction
               mma_mxf8f6f4_pair(acc, adesc0 + soff + 2 * jj, bdesc0 + soff + 2 * jj,
-                                idesc0 + (uint32_t)jj * kSfIdStep, slot, slot + 4, (kb + i > 0 || jj > 0) ? 1u : 0u);
+                                idesc0 + (uint32_t)jj * kSfIdStep, slot[i], slot[i] + 4,
+                                (kb + i > 0 || jj > 0) ? 1u : 0u);
           }
           tc_commit_pair(&empty[bar], 0x3);
           if (++bar == kPBars) {
