@@ -87,9 +87,9 @@ def measured_traffic(kernel: str):
     try:
         with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as fh:
             rec = json.load(fh)
-        src = os.path.join(ROOT, "quantized_moe_expert_top_gb300", "csrc", "prefill.cu")
+        src = os.path.join(ROOT, "quantized_moe_expert_top_gb300", "csrc", "gemm_pair.cu")
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if sha != rec.get("prefill_cu_sha256_16"):
+        if sha != rec.get("gemm_pair_cu_sha256_16"):
             return None
         return rec.get(kernel)
     except (OSError, ValueError):
@@ -275,7 +275,8 @@ def run_ours(args):
 
     wl = synth.WORKLOADS[args.workload]
     base = synth.WORKLOADS["prefill"]  # one layer serves decode1 / decode64 / prefill
-    layer_wl = wl if wl.down == "q2k" else base
+    # the decode and prefill workloads share one layer; a workload of another shape brings its own
+    layer_wl = base if (wl.down, wl.d, wl.E, wl.f, wl.k) == (base.down, base.d, base.E, base.f, base.k) else wl
     W = synth.make_layer_weights(layer_wl, device="cuda")
     layer = ds4.Layer(layer_wl.d, layer_wl.E, layer_wl.f, layer_wl.k, max(4096, wl.T), W)
     del W
@@ -469,7 +470,8 @@ def run_reference(args):
     if rank != 0:
         return
     wl = synth.WORKLOADS[args.workload]
-    layer_wl = wl if wl.down == "q2k" else synth.WORKLOADS["prefill"]
+    base = synth.WORKLOADS["prefill"]
+    layer_wl = base if (wl.down, wl.d, wl.E, wl.f, wl.k) == (base.down, base.d, base.E, base.f, base.k) else wl
     Wh = oracle_weights(layer_wl)
     per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):

@@ -84,6 +84,10 @@ WORKLOADS = {
     "decode64": Workload("decode64", 64, 4096, 256, 2048, 8, 2, 1, "zipf"),
     "prefill": Workload("prefill", 4096, 4096, 256, 2048, 8, 3, 1, "normal"),
     "q2k": Workload("q2k", 2048, 4096, 256, 2048, 8, 4, 4, "normal", "q2k"),
+    # profiling case: the prefill layer with 32 experts and 512 tokens, so each
+    # expert still receives about 128 tokens (the per-expert GEMM shape of the
+    # 4096-token chunk) while the device holds well under 1 GB
+    "prefill_e32": Workload("prefill_e32", 512, 4096, 32, 2048, 8, 3, 1, "normal"),
 }
 
 
