@@ -180,14 +180,15 @@ int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
  * forward also records a CUDA event on its stream before its first kernel and
  * after each kernel.  ds4moe_kernel_times() synchronises that stream and writes
  * the elapsed milliseconds of each kernel of the most recent forward, in
- * launch order (DECODE: route_topk, route_group, decode_gateup, decode_down;
- * PREFILL and DECODE_MMA: route_topk, route_group, act_quant, gemm_gateup,
- * gemm_down), and
- * returns how many it wrote (at most max_n), or a negative error.
- * ds4moe_kernel_name() gives those names (NULL past the end). */
+ * launch order, and returns how many it wrote (at most max_n), or a negative
+ * error.  ds4moe_kernel_name(layer, T, i) names the i-th kernel a forward of
+ * T tokens enqueues (NULL past the end):
+ *   DECODE:                route_topk, route_group, decode_gateup, decode_down
+ *   other paths, T <= 4:   route_small, gemm_gateup, gemm_down
+ *   other paths, T > 4:    route_topk, route_group, act_quant, gemm_gateup, gemm_down */
 int ds4moe_set_kernel_timing(ds4moe_layer *layer, int enable);
 int ds4moe_kernel_times(ds4moe_layer *layer, float *ms, int max_n);
-const char *ds4moe_kernel_name(int path, int i);
+const char *ds4moe_kernel_name(const ds4moe_layer *layer, int32_t T, int i);
 
 /* Routing alone (steps 1-2 above), allocating nothing.  The pages have no
  * counterpart: this call exists for callers that cannot allocate device

@@ -88,7 +88,7 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_kernel_times.restype = ctypes.c_int
         L.ds4moe_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         L.ds4moe_kernel_name.restype = ctypes.c_char_p
-        L.ds4moe_kernel_name.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.ds4moe_kernel_name.argtypes = [vp, i32, ctypes.c_int]
         L.ds4moe_route_noalloc.restype = ctypes.c_int
         L.ds4moe_route_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.ds4moe_status_string.restype = ctypes.c_char_p
@@ -243,8 +243,7 @@ class Layer:
         n = lib().ds4moe_kernel_times(self._h, buf, 8)
         if n < 0:
             raise Ds4moeError(n, "ds4moe_kernel_times")
-        path = self.path_for(self._last_T)
-        return {lib().ds4moe_kernel_name(path, i).decode(): float(buf[i]) for i in range(n)}
+        return {lib().ds4moe_kernel_name(self._h, self._last_T, i).decode(): float(buf[i]) for i in range(n)}
 
     def close(self):
         if self._h is not None:

@@ -377,6 +377,5 @@ cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStr
                     (uint64_t)L->cfg.wait_timeout_ms * 1000000ull);
 }
 
-int decode_launches() { return 4; }
 
 }  // namespace ds4moe

@@ -31,6 +31,42 @@ __device__ __forceinline__ int mxfp8_exponent(float amax) {
   return amax > 0.f ? max(-127, min(127, floor_log2_f32(amax) - 8)) : 0;
 }
 
+// MXFP8 of one 32-value block: E8M0 exponent s (floor(log2 amax) - 8, clamped;
+// 0 for an all-zero block) and the 32 codes packed little-endian in 8 words.
+__device__ __forceinline__ int mxfp8_block(const float (&v)[32], uint32_t (&packed)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mxfp8_exponent(amax);
+  const float inv = exp2i(-s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
+    const uint32_t hi = f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    packed[i] = lo | (hi << 16);
+  }
+  return s;
+}
+
+// MXFP8 of a block and of its residual: hi = MXFP8(v) (returned exponent,
+// codes in hi), lo = MXFP8(v - hi) (exponent in s_lo, codes in lo), so that
+// hi + lo carries about twice the E4M3 mantissa.  v is overwritten by the
+// residual.
+__device__ __forceinline__ int mxfp8_split_block(float (&v)[32], uint32_t (&hi)[8], uint32_t (&lo)[8], int& s_lo) {
+  const int s = mxfp8_block(v, hi);
+  const float sc = exp2i(s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 a = e4m3x2_to_f32x2(hi[i] & 0xFFFFu), b = e4m3x2_to_f32x2(hi[i] >> 16);
+    v[4 * i] -= a.x * sc;
+    v[4 * i + 1] -= a.y * sc;
+    v[4 * i + 2] -= b.x * sc;
+    v[4 * i + 3] -= b.y * sc;
+  }
+  s_lo = mxfp8_block(v, lo);
+  return s;
+}
+
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: A/B formats
 // (E4M3 = 0, E2M1 = 5), K-major A and B, N >> 3, E8M0 scales, M >> 4, and the
 // byte of the 32-bit scale word (one per 32-K step) used for A and B.

@@ -40,6 +40,7 @@ constexpr int kGateUpNMax = 224;  // token columns per gate/up tile (two accumul
 constexpr int kDownNMax = 256;    // token columns per down tile
 constexpr int kQ2kChunk = 3072;   // bytes of one Q2_K tile-major chunk
 constexpr int kNumBoxMaps = 12;   // token-tile TMA maps with 16, 32, ..., 192-row boxes
+constexpr int kSmallRouteT = 4;  // largest T routed (and its activations quantised) by the single-block kernel
 
 // Routing tables and scratch for one forward call (all device memory).
 struct Scratch {
@@ -123,6 +124,10 @@ namespace ds4moe {
 cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
                               cudaStream_t st);
 cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream_t st);
+// Few-token routing (T <= kSmallRouteT) in one launch, with the activation
+// quantisation and the zeroing of out when `quant` is set.
+cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const void* x, float* out, int T, int split,
+                               bool quant, cudaStream_t st);
 
 cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st);
 cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
@@ -142,7 +147,5 @@ cudaError_t launch_repack_q2k(const uint8_t* blocks, ds4moe_layer* L, cudaStream
 cudaError_t launch_pack_rows(uint8_t* dst, int pitch, int64_t rows, const uint8_t* s0, int l0, const uint8_t* s1,
                              int l1, const uint8_t* s2, int l2, const uint8_t* s3, int l3, cudaStream_t st);
 
-int decode_launches();
-int prefill_launches();
 
 }  // namespace ds4moe

@@ -194,6 +194,22 @@ int path_of(const ds4moe_layer* L, int T) {
   return T <= L->cfg.decode_max_tokens ? DS4MOE_PATH_DECODE_MMA : DS4MOE_PATH_PREFILL;
 }
 
+// Names of the kernels one forward of T tokens enqueues, in launch order.
+int kernel_list(const ds4moe_layer* L, int T, const char** names) {
+  int n = 0;
+  const int path = path_of(L, T);
+  if (path == DS4MOE_PATH_DECODE) {
+    for (const char* k : {"route_topk", "route_group", "decode_gateup", "decode_down"}) names[n++] = k;
+  } else if (T <= kSmallRouteT) {
+    names[n++] = "route_small";
+    names[n++] = "gemm_gateup";
+    names[n++] = "gemm_down";
+  } else {
+    for (const char* k : {"route_topk", "route_group", "act_quant", "gemm_gateup", "gemm_down"}) names[n++] = k;
+  }
+  return n;
+}
+
 void free_all(ds4moe_layer* L) {
   for (int i = 0; i < L->n_owned; ++i) cudaFree(L->owned[i]);
   L->n_owned = 0;
@@ -411,7 +427,8 @@ int ds4moe_launches_per_forward(const ds4moe_layer* L, int32_t T) {
   const int p = ds4moe_path_for(L, T);
   if (p < 0) return p;
   if (T == 0) return 0;
-  return p == DS4MOE_PATH_DECODE ? decode_launches() : prefill_launches();
+  const char* names[8];
+  return kernel_list(L, T, names);
 }
 
 int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
@@ -441,14 +458,20 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   };
   cudaError_t e = L->timing ? cudaEventRecord(L->ev[0], st) : cudaSuccess;
   nk = 1;
-  if (e == cudaSuccess)
-    e = mark(launch_route_topk(L, logits, x, path == DS4MOE_PATH_DECODE, T, st));
-  if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
   if (path == DS4MOE_PATH_DECODE) {
+    if (e == cudaSuccess) e = mark(launch_route_topk(L, logits, x, true, T, st));
+    if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
     if (e == cudaSuccess) e = mark(launch_decode_gateup(L, x, out, T, st));
     if (e == cudaSuccess) e = mark(launch_decode_down(L, out, T, st));
   } else {
-    if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, split, st));
+    if (T <= kSmallRouteT) {
+      // routing and the activations in one launch
+      if (e == cudaSuccess) e = mark(launch_route_small(L, logits, x, out, T, split, true, st));
+    } else {
+      if (e == cudaSuccess) e = mark(launch_route_topk(L, logits, x, false, T, st));
+      if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
+      if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, split, st));
+    }
     if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, split, st));
     if (e == cudaSuccess) {
       if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = mark(launch_gemm_down_q2k(L, out, T, st));
@@ -554,12 +577,11 @@ int ds4moe_kernel_times(ds4moe_layer* L, float* ms, int max_n) {
   return n;
 }
 
-const char* ds4moe_kernel_name(int path, int i) {
-  static const char* dec[] = {"route_topk", "route_group", "decode_gateup", "decode_down"};
-  static const char* pre[] = {"route_topk", "route_group", "act_quant", "gemm_gateup", "gemm_down"};
-  if (path == DS4MOE_PATH_DECODE && i >= 0 && i < 4) return dec[i];
-  if ((path == DS4MOE_PATH_PREFILL || path == DS4MOE_PATH_DECODE_MMA) && i >= 0 && i < 5) return pre[i];
-  return nullptr;
+const char* ds4moe_kernel_name(const ds4moe_layer* L, int32_t T, int i) {
+  if (!L || T <= 0 || T > L->cfg.max_tokens || i < 0) return nullptr;
+  const char* names[8];
+  const int n = kernel_list(L, T, names);
+  return i < n ? names[i] : nullptr;
 }
 
 void ds4moe_destroy(ds4moe_layer* L) {

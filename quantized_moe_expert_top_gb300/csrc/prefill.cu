@@ -23,91 +23,65 @@ namespace ds4moe {
 namespace {
 
 // --------------------------------------------------------------- MXFP8 of x
-// One warp per token.  Lane l quantises blocks l, l+32, ... of x[t] (32 bf16
-// each) to E4M3 with one E8M0 scale (s = floor(log2 amax) - 8, clamped; 0 for
-// an all-zero block), then writes the codes and the scale to the k padded rows
-// of the token's routed pairs.  Also zeroes out[t] for the down epilogue.
-// MXFP8 of one 32-value block: E8M0 exponent s (floor(log2 amax) - 8, clamped;
-// 0 for an all-zero block) and the 32 codes packed little-endian in 8 words.
-__device__ __forceinline__ int mxfp8_block(const float (&v)[32], uint32_t (&packed)[8]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int s = mxfp8_exponent(amax);
-  const float inv = exp2i(-s);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t lo = f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
-    const uint32_t hi = f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-    packed[i] = lo | (hi << 16);
-  }
-  return s;
-}
-
+// One warp per (token, 1024 elements): lane l quantises one block of 32 bf16
+// to E4M3 with one E8M0 scale (s = floor(log2 amax) - 8, clamped; 0 for an
+// all-zero block), then writes the codes and the scale to the k padded rows of
+// the token's routed pairs (and the residual as a second row when split).
+// Also zeroes the warp's part of out[t] for the down epilogue.
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k,
                                                         const int32_t* __restrict__ pad_inv, uint8_t* __restrict__ xq,
                                                         uint8_t* __restrict__ xsf, int r128, int split,
                                                         float* __restrict__ out) {
   pdl_wait();
   pdl_launch_dependents();
-  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  // one warp per (token, 32 consecutive blocks of 32 elements); lane = block
+  const int nblk = d / 32, parts = (nblk + 31) / 32;
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
+  const int t = gw / parts, part = gw % parts;
   if (t >= T) return;
   {
-    float4* o = reinterpret_cast<float4*>(out + (size_t)t * d);
-    for (int i = lane; i < d / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* o = reinterpret_cast<float4*>(out + (size_t)t * d + (size_t)part * 1024);
+    const int n4 = min(1024, d - part * 1024) / 4;
+    for (int i = lane; i < n4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  const int c = part * 32 + lane;
+  if (c >= nblk) return;
   int rows[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(pad_inv + (size_t)t * k + j) : 0;
-  const int nblk = d / 32;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-  for (int c = lane; c < nblk; c += 32) {
-    float v[32];
+  float v[32];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = __ldg(src + 4 * c + q);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = __ldg(src + 4 * c + q);
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        v[8 * q + 2 * h] = __uint_as_float(wv[h] << 16);
-        v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
-      }
+    for (int h = 0; h < 4; ++h) {
+      v[8 * q + 2 * h] = __uint_as_float(wv[h] << 16);
+      v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
     }
-    uint32_t packed[8], packed_lo[8];
-    const int s = mxfp8_block(v, packed);
-    int s_lo = 0;
-    if (split == 2) {  // residual after the hi codes, quantised the same way
-      const float sc = exp2i(s);
+  }
+  uint32_t packed[8], packed_lo[8];
+  int s_lo = 0;
+  const int s = split == 2 ? mxfp8_split_block(v, packed, packed_lo, s_lo) : mxfp8_block(v, packed);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 a = e4m3x2_to_f32x2(packed[i] & 0xFFFFu), b = e4m3x2_to_f32x2(packed[i] >> 16);
-        v[4 * i] -= a.x * sc;
-        v[4 * i + 1] -= a.y * sc;
-        v[4 * i + 2] -= b.x * sc;
-        v[4 * i + 3] -= b.y * sc;
-      }
-      s_lo = mxfp8_block(v, packed_lo);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
-        const size_t r = (size_t)rows[j];
-        uint4* dst = reinterpret_cast<uint4*>(xq + r * d + 32 * (size_t)c);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        xsf[act_sf_index(r, c, r128)] = (uint8_t)(s + 127);
-        if (split == 2) {
-          uint4* dlo = reinterpret_cast<uint4*>(xq + (r + 1) * d + 32 * (size_t)c);
-          dlo[0] = make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
-          dlo[1] = make_uint4(packed_lo[4], packed_lo[5], packed_lo[6], packed_lo[7]);
-          xsf[act_sf_index(r + 1, c, r128)] = (uint8_t)(s_lo + 127);
-        }
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      const size_t r = (size_t)rows[j];
+      uint4* dst = reinterpret_cast<uint4*>(xq + r * d + 32 * (size_t)c);
+      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      xsf[act_sf_index(r, c, r128)] = (uint8_t)(s + 127);
+      if (split == 2) {
+        uint4* dlo = reinterpret_cast<uint4*>(xq + (r + 1) * d + 32 * (size_t)c);
+        dlo[0] = make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
+        dlo[1] = make_uint4(packed_lo[4], packed_lo[5], packed_lo[6], packed_lo[7]);
+        xsf[act_sf_index(r + 1, c, r128)] = (uint8_t)(s_lo + 127);
       }
     }
   }
 }
-
 
 // --------------------------------------------------------------- Q2_K down GEMM
 // Tensor memory (512 columns): accumulator buffers at columns 0 and 256.  One
@@ -504,7 +478,8 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, int split, cudaStream_t st) {
-  const int blocks = (T + 7) / 8;
+  const int parts = (L->cfg.d_model / 32 + 31) / 32;  // warps per token
+  const int blocks = (T * parts + 7) / 8;
   return launch_pdl(act_quant_kernel, blocks, 256, 0, st, static_cast<const __nv_bfloat16*>(x), T, L->cfg.d_model,
                     L->cfg.top_k, L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), split, out);
 }
@@ -539,6 +514,5 @@ cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaS
   return launch_pdl(q2k_down_kernel, grid, kQThreads, QSmem::kTotal, st, maps, a);
 }
 
-int prefill_launches() { return 5; }
 
 }  // namespace ds4moe

@@ -7,6 +7,7 @@
 // layer's specification: the k largest fp32 logits per token ordered by
 // (value desc, expert index asc), weights = softmax over those k only.
 #include "common.cuh"
+#include "gemm.cuh"
 #include "internal.h"
 
 #include <math.h>
@@ -58,17 +59,12 @@ __device__ __forceinline__ void prepare_x_f16(const __nv_bfloat16* __restrict__ 
   }
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int32_t* __restrict__ idx, float* __restrict__ w,
-                                                         const __nv_bfloat16* __restrict__ x, int d,
-                                                         uint4* __restrict__ xh, float* __restrict__ xsig) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int token = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (token >= T) return;
-  if (xh != nullptr) prepare_x_f16(x, token, d, xh, xsig, lane);
-  const float* row = logits + (size_t)token * E;
+// Top-k of one token's logits by one warp (lane l holds entries l, l+32, ...,
+// so a lane's own entries are in increasing index order); lane 0 writes the k
+// expert indices (value desc, index asc) and their softmax weights to idx[0..k)
+// and w[0..k).
+__device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k, int lane,
+                                          int32_t* __restrict__ idx, float* __restrict__ w) {
 
   float v[kMaxE / 32];
   uint32_t taken = 0;  // bit i: entry lane+32i already selected, or beyond E
@@ -124,11 +120,24 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j < k) {
-        idx[(size_t)token * k + j] = sel_e[j];
-        w[(size_t)token * k + j] = expf(sel_v[j] - sel_v[0]) / z;
+        idx[j] = sel_e[j];
+        w[j] = expf(sel_v[j] - sel_v[0]) / z;
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ idx, float* __restrict__ w,
+                                                         const __nv_bfloat16* __restrict__ x, int d,
+                                                         uint4* __restrict__ xh, float* __restrict__ xsig) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int token = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (token >= T) return;
+  if (xh != nullptr) prepare_x_f16(x, token, d, xh, xsig, lane);
+  topk_warp(logits + (size_t)token * E, E, k, lane, idx + (size_t)token * k, w + (size_t)token * k);
 }
 
 // Inclusive scan of one int per thread over a 256-thread block.
@@ -244,6 +253,109 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   }
 }
 
+// Few-token routing in one block of 1024 threads (T <= kSmallRouteT): top-k
+// of every token (one warp per token), then the grouping of route_group_kernel
+// done in shared memory (histogram, scans, and the rank of pair (t, j) among
+// the earlier tokens that chose the same expert), and, when `quant` is set,
+// the MXFP8 quantisation of x into the routed pairs' rows (hi + lo rows when
+// split == 2) and the zeroing of out, so that a decode step needs one launch
+// before its GEMMs.
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx, float* __restrict__ w,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ pad_offsets,
+    int32_t* __restrict__ perm_tok, int32_t* __restrict__ perm_slot, int32_t* __restrict__ inv,
+    int32_t* __restrict__ pad_inv, int32_t* __restrict__ pad_pair, int32_t* __restrict__ touched, int split,
+    const __nv_bfloat16* __restrict__ x, int d, uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, int r128,
+    float* __restrict__ out, int quant) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_idx[kSmallRouteT * kMaxK];
+  __shared__ int s_prow[kSmallRouteT * kMaxK];
+  __shared__ int hist[kMaxE], s_off[kMaxE], s_poff[kMaxE];
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int npairs = T * k;
+
+  for (int t = wid; t < T; t += (int)(blockDim.x >> 5))
+    topk_warp(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
+  for (int e = tid; e < kMaxE; e += blockDim.x) hist[e] = 0;
+  __syncthreads();  // the block's global writes above are visible to the block from here
+  for (int p = tid; p < npairs; p += blockDim.x) {
+    const int e = idx[p];
+    s_idx[p] = e;
+    atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+
+  // exclusive scans of counts, padded counts and the touched flag (tid = expert)
+  const int c = (tid < E) ? hist[tid] : 0;
+  const int pc = (c * split + kPadRows - 1) / kPadRows * kPadRows;
+  const int inc_c = block_scan_incl(c, warp_tot);
+  const int inc_pc = block_scan_incl(pc, warp_tot);
+  const int inc_t = block_scan_incl(c > 0 ? 1 : 0, warp_tot);
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = s_off[tid] = inc_c - c;
+    pad_offsets[tid] = s_poff[tid] = inc_pc - pc;
+    if (c > 0) touched[inc_t - 1] = tid;
+    if (tid == E - 1) {
+      offsets[E] = inc_c;
+      pad_offsets[E] = inc_pc;
+      touched[E] = inc_t;
+    }
+  }
+  __syncthreads();
+
+  for (int p = tid; p < npairs; p += blockDim.x) {
+    const int t = p / k, j = p % k, e = s_idx[p];
+    int r = 0;  // earlier tokens that chose e (a token chooses an expert at most once)
+    for (int q = 0; q < t * k; ++q) r += (s_idx[q] == e) ? 1 : 0;
+    const int pos = s_off[e] + r, ppos = s_poff[e] + r * split;
+    perm_tok[pos] = t;
+    perm_slot[pos] = j;
+    inv[p] = pos;
+    pad_inv[p] = ppos;
+    for (int q = 0; q < split; ++q) pad_pair[ppos + q] = p;
+    s_prow[p] = ppos;
+  }
+  if (!quant) return;
+  __syncthreads();
+
+  const int nblk = d / 32;
+  for (int task = tid; task < npairs * nblk; task += blockDim.x) {
+    const int j = task % k, tb = task / k;
+    const int t = tb / nblk, cb = tb % nblk;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d) + 4 * cb;
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(src + q);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v[8 * q + 2 * h] = __uint_as_float(wv[h] << 16);
+        v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+      }
+    }
+    uint32_t hi[8], lo[8];
+    int s_lo = 0;
+    const int s_hi = split == 2 ? mxfp8_split_block(v, hi, lo, s_lo) : mxfp8_block(v, hi);
+    const size_t row = (size_t)s_prow[t * k + j];
+    uint4* dst = reinterpret_cast<uint4*>(xq + row * d + 32 * (size_t)cb);
+    dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    dst[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    xsf[act_sf_index(row, cb, r128)] = (uint8_t)(s_hi + 127);
+    if (split == 2) {
+      uint4* dlo = reinterpret_cast<uint4*>(xq + (row + 1) * d + 32 * (size_t)cb);
+      dlo[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      dlo[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+      xsf[act_sf_index(row + 1, cb, r128)] = (uint8_t)(s_lo + 127);
+    }
+  }
+  float4* o4 = reinterpret_cast<float4*>(out);
+  for (int i = tid; i < T * d / 4; i += blockDim.x) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
@@ -260,6 +372,16 @@ cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream
   const Scratch& s = L->s;
   return launch_pdl(route_group_kernel, E, 256, 0, st, s.topk_idx, T, E, k, s.counts, s.offsets, s.pad_offsets,
                     s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, rpp);
+}
+
+cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const void* x, float* out, int T, int split,
+                               bool quant, cudaStream_t st) {
+  const int E = L->cfg.n_experts, k = L->cfg.top_k;
+  const Scratch& s = L->s;
+  return launch_pdl(route_small_kernel, 1, 1024, 0, st, logits, T, E, k, s.topk_idx, s.topk_w, s.counts, s.offsets,
+                    s.pad_offsets, s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, split,
+                    static_cast<const __nv_bfloat16*>(x), L->cfg.d_model, s.xq, s.xsf, (int)(s.pad_rows_max / 128),
+                    out, quant ? 1 : 0);
 }
 
 }  // namespace ds4moe

@@ -54,8 +54,13 @@ def test_path_choice_and_launch_counts(ds4, tiny):
     assert layer.path_for(4) == ds4.PATH_DECODE_MMA
     assert layer.path_for(5) == ds4.PATH_PREFILL
     assert layer.path_for(17) == ds4.ERR_TOO_MANY_TOKENS
-    assert layer.launches_per_forward(4) == 5
+    # up to 4 tokens, routing and the activation quantisation are one launch
+    assert layer.launches_per_forward(4) == 3
     assert layer.launches_per_forward(16) == 5
+    names = [ds4.lib().ds4moe_kernel_name(layer._h, 4, i) for i in range(4)]
+    assert names == [b"route_small", b"gemm_gateup", b"gemm_down", None]
+    names = [ds4.lib().ds4moe_kernel_name(layer._h, 16, i) for i in range(6)]
+    assert names == [b"route_topk", b"route_group", b"act_quant", b"gemm_gateup", b"gemm_down", None]
 
 
 @pytest.mark.parametrize("T", [4, 16])
