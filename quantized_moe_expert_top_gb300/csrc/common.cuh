@@ -324,16 +324,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Each thread of the warp writes zeros to 16 consecutive 32-bit columns of its own lane.
-__device__ __forceinline__ void tmem_st_zero_32x32b_x16(uint32_t taddr) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};" ::"r"(taddr),
-      "r"(0u)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)
 // Two CTAs of a cluster share one tensor-core operation: CTA rank 0 (the
 // leader) issues it, each CTA supplies half of the A rows and half of the B
