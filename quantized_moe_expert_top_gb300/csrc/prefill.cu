@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
     for (int i = lane; i < n4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int c = part * 32 + lane;
+  // lanes past the row leave in whole groups of four (nblk % 4 == 0)
+  const unsigned vmask = __ballot_sync(0xffffffffu, c < nblk);
   if (c >= nblk) return;
   int rows[8];
 #pragma unroll
@@ -65,6 +67,14 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   uint32_t packed[8], packed_lo[8];
   int s_lo = 0;
   const int s = split == 2 ? mxfp8_split_block(v, packed, packed_lo, s_lo) : mxfp8_block(v, packed);
+  // The scales of blocks 4i .. 4i + 3 of a row are 4 consecutive bytes of its
+  // scale chunk: lane 4i gathers them and stores one word.
+  uint32_t sw = (uint32_t)(s + 127) << (8 * (lane & 3));
+  uint32_t sw_lo = (uint32_t)(s_lo + 127) << (8 * (lane & 3));
+  sw |= __shfl_xor_sync(vmask, sw, 1);
+  sw |= __shfl_xor_sync(vmask, sw, 2);
+  sw_lo |= __shfl_xor_sync(vmask, sw_lo, 1);
+  sw_lo |= __shfl_xor_sync(vmask, sw_lo, 2);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < k) {
@@ -72,12 +82,12 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
       uint4* dst = reinterpret_cast<uint4*>(xq + r * d + 32 * (size_t)c);
       dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
       dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      xsf[act_sf_index(r, c, r128)] = (uint8_t)(s + 127);
+      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xsf + act_sf_index(r, c, r128)) = sw;
       if (split == 2) {
         uint4* dlo = reinterpret_cast<uint4*>(xq + (r + 1) * d + 32 * (size_t)c);
         dlo[0] = make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
         dlo[1] = make_uint4(packed_lo[4], packed_lo[5], packed_lo[6], packed_lo[7]);
-        xsf[act_sf_index(r + 1, c, r128)] = (uint8_t)(s_lo + 127);
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xsf + act_sf_index(r + 1, c, r128)) = sw_lo;
       }
     }
   }

@@ -165,13 +165,17 @@ __device__ __forceinline__ int block_scan_incl(int v, int* warp_tot) {
   return v + add;
 }
 
-// Grid = E blocks of 256 threads; block e places expert e's pairs.
+// Grid = E blocks of 256 threads; block e places expert e's pairs in one
+// pass over idx: each thread takes a contiguous run of tokens, adds their
+// selections to the block's histogram of all experts and counts those equal
+// to e; then
 //   offsets[e]     = number of pairs with expert < e (exclusive scan of counts)
 //   pad_offsets[e] = same over rpp*counts rounded up to 128 rows (rpp = padded
 //                    rows per pair: 1, or 2 when x is split into hi + lo rows)
 //   rank of pair (t, j) with idx[t,j] == e = number of tokens t' < t that
-//   selected e (each token selects an expert at most once), so the order is
-//   (expert, token) and is independent of thread timing.
+//   selected e (each token selects an expert at most once): the exclusive
+//   scan of the threads' counts plus the order inside a thread's run, so the
+//   order is (expert, token) and is independent of thread timing.
 __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ pad_offsets,
@@ -187,11 +191,32 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   pdl_launch_dependents();
   const int e = blockIdx.x;
   const int tid = threadIdx.x;
-  const int npairs = T * k;
 
   for (int i = tid; i < kMaxE; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int p = tid; p < npairs; p += blockDim.x) atomicAdd(&hist[__ldg(idx + p)], 1);
+  const int per = (T + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int t0 = min(T, tid * per), t1 = min(T, t0 + per);
+  const bool vec = (k % 4) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0;
+  int hits = 0;
+  for (int t = t0; t < t1; ++t) {
+    const int32_t* row = idx + (size_t)t * k;
+    if (vec) {
+      for (int j = 0; j < k; j += 4) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(row + j));
+        atomicAdd(&hist[v.x], 1);
+        atomicAdd(&hist[v.y], 1);
+        atomicAdd(&hist[v.z], 1);
+        atomicAdd(&hist[v.w], 1);
+        hits += (v.x == e) + (v.y == e) + (v.z == e) + (v.w == e);
+      }
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const int v = __ldg(row + j);
+        atomicAdd(&hist[v], 1);
+        hits += v == e;
+      }
+    }
+  }
   __syncthreads();
 
   // exclusive scans of counts, padded counts and the touched flag (tid = expert)
@@ -215,41 +240,24 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
       touched[E] = inc_t;
     }
   }
-  __syncthreads();
+  // rank of this thread's first selection of e (the scan's barriers also
+  // publish s_off and s_poff)
+  int r = block_scan_incl(hits, warp_tot) - hits;
   const int off = s_off, poff = s_poff;
-
-  // rank assignment for expert e, 256 tokens at a time
-  const int lane = tid & 31, wid = tid >> 5;
-  int running = 0;
-  for (int base = 0; base < T; base += blockDim.x) {
-    const int t = base + tid;
-    int slot = -1;
-    if (t < T) {
-      for (int j = 0; j < k; ++j)
-        if (__ldg(idx + (size_t)t * k + j) == e) slot = j;
-    }
-    const unsigned ball = __ballot_sync(0xffffffffu, slot >= 0);
-    const int in_warp = __popc(ball & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[wid] = __popc(ball);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
-      const int n = warp_tot[q];
-      if (q < wid) before += n;
-      total += n;
-    }
-    if (slot >= 0) {
-      const int r = running + before + in_warp;
+  for (int t = t0; t < t1 && hits > 0; ++t) {
+    const int32_t* row = idx + (size_t)t * k;
+    for (int j = 0; j < k; ++j) {
+      if (__ldg(row + j) != e) continue;
       const int pos = off + r, ppos = poff + r * rpp;
-      const int pair = t * k + slot;
+      const int pair = t * k + j;
       perm_tok[pos] = t;
-      perm_slot[pos] = slot;
+      perm_slot[pos] = j;
       inv[pair] = pos;
       pad_inv[pair] = ppos;
       for (int q = 0; q < rpp; ++q) pad_pair[ppos + q] = pair;
+      ++r;
+      --hits;
     }
-    running += total;
-    __syncthreads();
   }
 }
 
