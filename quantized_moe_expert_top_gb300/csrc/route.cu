@@ -196,25 +196,40 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   __syncthreads();
   const int per = (T + (int)blockDim.x - 1) / (int)blockDim.x;
   const int t0 = min(T, tid * per), t1 = min(T, t0 + per);
-  const bool vec = (k % 4) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0;
+  // the thread's selections idx[t0 * k .. t1 * k) are contiguous
+  const int p0 = t0 * k, p1 = t1 * k;
   int hits = 0;
-  for (int t = t0; t < t1; ++t) {
-    const int32_t* row = idx + (size_t)t * k;
-    if (vec) {
-      for (int j = 0; j < k; j += 4) {
-        const int4 v = __ldg(reinterpret_cast<const int4*>(row + j));
-        atomicAdd(&hist[v.x], 1);
-        atomicAdd(&hist[v.y], 1);
-        atomicAdd(&hist[v.z], 1);
-        atomicAdd(&hist[v.w], 1);
-        hits += (v.x == e) + (v.y == e) + (v.z == e) + (v.w == e);
+  if ((k % 4) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
+    // eight 16-byte loads in flight per round
+    const int4* v4 = reinterpret_cast<const int4*>(idx + p0);
+    const int n4 = (p1 - p0) / 4;
+    int i = 0;
+    for (; i + 8 <= n4; i += 8) {
+      int4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(v4 + i + u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        atomicAdd(&hist[v[u].x], 1);
+        atomicAdd(&hist[v[u].y], 1);
+        atomicAdd(&hist[v[u].z], 1);
+        atomicAdd(&hist[v[u].w], 1);
+        hits += (v[u].x == e) + (v[u].y == e) + (v[u].z == e) + (v[u].w == e);
       }
-    } else {
-      for (int j = 0; j < k; ++j) {
-        const int v = __ldg(row + j);
-        atomicAdd(&hist[v], 1);
-        hits += v == e;
-      }
+    }
+    for (; i < n4; ++i) {
+      const int4 v = __ldg(v4 + i);
+      atomicAdd(&hist[v.x], 1);
+      atomicAdd(&hist[v.y], 1);
+      atomicAdd(&hist[v.z], 1);
+      atomicAdd(&hist[v.w], 1);
+      hits += (v.x == e) + (v.y == e) + (v.z == e) + (v.w == e);
+    }
+  } else {
+    for (int p = p0; p < p1; ++p) {
+      const int v = __ldg(idx + p);
+      atomicAdd(&hist[v], 1);
+      hits += v == e;
     }
   }
   __syncthreads();
@@ -244,20 +259,16 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   // publish s_off and s_poff)
   int r = block_scan_incl(hits, warp_tot) - hits;
   const int off = s_off, poff = s_poff;
-  for (int t = t0; t < t1 && hits > 0; ++t) {
-    const int32_t* row = idx + (size_t)t * k;
-    for (int j = 0; j < k; ++j) {
-      if (__ldg(row + j) != e) continue;
-      const int pos = off + r, ppos = poff + r * rpp;
-      const int pair = t * k + j;
-      perm_tok[pos] = t;
-      perm_slot[pos] = j;
-      inv[pair] = pos;
-      pad_inv[pair] = ppos;
-      for (int q = 0; q < rpp; ++q) pad_pair[ppos + q] = pair;
-      ++r;
-      --hits;
-    }
+  for (int pair = p0; pair < p1 && hits > 0; ++pair) {
+    if (__ldg(idx + pair) != e) continue;
+    const int pos = off + r, ppos = poff + r * rpp;
+    perm_tok[pos] = pair / k;
+    perm_slot[pos] = pair % k;
+    inv[pair] = pos;
+    pad_inv[pair] = ppos;
+    for (int q = 0; q < rpp; ++q) pad_pair[ppos + q] = pair;
+    ++r;
+    --hits;
   }
 }
 
