@@ -171,27 +171,47 @@ __device__ __forceinline__ void gateup_slice(const uint32_t (&r)[16], bool gate,
   for (int jj = 0; jj < kHalf; ++jj) h[jj] = gate ? v[jj] * su[jj * 32 + lane] : sg[jj * 32 + lane] * v[kHalf + jj];
   named_bar_sync(6 + pid, 64);  // staging free for the next slice
   const int tok0 = c0 / SPLIT + (gate ? 0 : kHalf);  // first token of this warp's half
+  // amax of a 32-feature block (the warp's lanes) for all of the warp's
+  // tokens at once: a butterfly of shuffles on the magnitudes' bit patterns
+  // (unsigned order = float order for non-negative values); lane j then stores
+  // the scale byte of token j, one store for all tokens.
+  auto block_amax = [&](uint32_t (&am)[kHalf]) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int jj = 0; jj < kHalf; ++jj) am[jj] = max(am[jj], __shfl_xor_sync(0xffffffffu, am[jj], o));
+  };
   if constexpr (SPLIT == 2) {
+    uint32_t am[kHalf], am2[kHalf], chi[kHalf];
+    int s[kHalf];
+    float res[kHalf];
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) am[jj] = __float_as_uint(fabsf(h[jj]));
+    block_amax(am);
 #pragma unroll
     for (int jj = 0; jj < kHalf; ++jj) {
-      const float a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj]))));
-      const int s = mxfp8_exponent(a);
-      const uint32_t chi = f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu;
-      const float res = h[jj] - e4m3x2_to_f32x2(chi).x * exp2i(s);
-      const float a2 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(res))));
-      const int s2 = mxfp8_exponent(a2);
-      const uint32_t clo = f32x2_to_e4m3x2(res * exp2i(-s2), 0.f) & 0xFFu;
+      s[jj] = mxfp8_exponent(__uint_as_float(am[jj]));
+      chi[jj] = f32x2_to_e4m3x2(h[jj] * exp2i(-s[jj]), 0.f) & 0xFFu;
+      res[jj] = h[jj] - e4m3x2_to_f32x2(chi[jj]).x * exp2i(s[jj]);
+      am2[jj] = __float_as_uint(fabsf(res[jj]));
+    }
+    block_amax(am2);
+    uint32_t sf_mine = 0;  // lane 2j: scale of token j's hi row, lane 2j + 1: of its lo row
+#pragma unroll
+    for (int jj = 0; jj < kHalf; ++jj) {
+      const int s2 = mxfp8_exponent(__uint_as_float(am2[jj]));
+      const uint32_t clo = f32x2_to_e4m3x2(res[jj] * exp2i(-s2), 0.f) & 0xFFu;
+      if (lane == 2 * jj) sf_mine = (uint32_t)(s[jj] + 127);
+      if (lane == 2 * jj + 1) sf_mine = (uint32_t)(s2 + 127);
       const int col = 2 * (tok0 + jj);
       if (col < nch) {
         const size_t row = (size_t)(prow + col);
-        args.hq[row * args.f + i] = (uint8_t)chi;
+        args.hq[row * args.f + i] = (uint8_t)chi[jj];
         args.hq[(row + 1) * args.f + i] = (uint8_t)clo;
-        if (lane == 0) {
-          args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
-          args.hsf[act_sf_index(row + 1, i / 32, args.r128)] = (uint8_t)(s2 + 127);
-        }
       }
     }
+    if (lane < 2 * kHalf && 2 * tok0 + lane < nch)
+      args.hsf[act_sf_index((size_t)(prow + 2 * tok0 + lane), i / 32, args.r128)] = (uint8_t)sf_mine;
   } else {
     if (args.h16 != nullptr) {
 #pragma unroll
@@ -199,19 +219,21 @@ __device__ __forceinline__ void gateup_slice(const uint32_t (&r)[16], bool gate,
         if (tok0 + jj < nch) args.h16[(size_t)(prow + tok0 + jj) * args.f + i] = __float2half_rn(h[jj]);
       return;
     }
-    uint32_t amax[kHalf];
+    uint32_t am[kHalf];
 #pragma unroll
-    for (int jj = 0; jj < kHalf; ++jj) amax[jj] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[jj])));
+    for (int jj = 0; jj < kHalf; ++jj) am[jj] = __float_as_uint(fabsf(h[jj]));
+    block_amax(am);
+    uint32_t sf_mine = 0;  // lane j: scale of token j
 #pragma unroll
     for (int jj = 0; jj < kHalf; ++jj) {
+      const int s = mxfp8_exponent(__uint_as_float(am[jj]));
+      if (lane == jj) sf_mine = (uint32_t)(s + 127);
       const int col = tok0 + jj;
-      if (col < nch) {
-        const int s = mxfp8_exponent(__uint_as_float(amax[jj]));
-        const size_t row = (size_t)(prow + col);
-        args.hq[row * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
-        if (lane == 0) args.hsf[act_sf_index(row, i / 32, args.r128)] = (uint8_t)(s + 127);
-      }
+      if (col < nch)
+        args.hq[(size_t)(prow + col) * args.f + i] = (uint8_t)(f32x2_to_e4m3x2(h[jj] * exp2i(-s), 0.f) & 0xFFu);
     }
+    if (lane < kHalf && tok0 + lane < nch)
+      args.hsf[act_sf_index((size_t)(prow + tok0 + lane), i / 32, args.r128)] = (uint8_t)sf_mine;
   }
 }
 
