@@ -272,13 +272,85 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   }
 }
 
-// Few-token routing in one block of 1024 threads (T <= kSmallRouteT): top-k
-// of every token (one warp per token), then the grouping of route_group_kernel
-// done in shared memory (histogram, scans, and the rank of pair (t, j) among
-// the earlier tokens that chose the same expert), and, when `quant` is set,
-// the MXFP8 quantisation of x into the routed pairs' rows (hi + lo rows when
-// split == 2) and the zeroing of out, so that a decode step needs one launch
-// before its GEMMs.
+// Grouping of the T*k <= 32 pairs of a few-token call by one warp, without
+// block barriers: lane p holds pair p; experts e = lane + 32i are counted and
+// scanned in order with warp scans; the rank of pair p is the number of earlier
+// pairs with the same expert (a token selects an expert at most once, so these
+// are earlier tokens).  The same tables as route_group_kernel, and s_prow[p] =
+// the pair's first padded row.
+__device__ __forceinline__ void group_warp(const int32_t* idx, int npairs, int E, int k, int rpp, int lane,
+                                           int32_t* counts, int32_t* offsets, int32_t* pad_offsets, int32_t* perm_tok,
+                                           int32_t* perm_slot, int32_t* inv, int32_t* pad_inv, int32_t* pad_pair,
+                                           int32_t* touched, int* s_off, int* s_poff, int* s_prow) {
+  const int ep = lane < npairs ? idx[lane] : -1;
+  int cnt[kMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) cnt[i] = 0;
+  for (int q = 0; q < npairs; ++q) {
+    const int eq = __shfl_sync(0xffffffffu, ep, q);
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) cnt[i] += (eq == lane + 32 * i) ? 1 : 0;
+  }
+  int base_c = 0, base_pc = 0, base_t = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    const int e = lane + 32 * i;
+    const int c = e < E ? cnt[i] : 0;
+    const int pc = (c * rpp + kPadRows - 1) / kPadRows * kPadRows;
+    const int tf = c > 0 ? 1 : 0;
+    int ic = c, ipc = pc, it = tf;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nc = __shfl_up_sync(0xffffffffu, ic, o), npc = __shfl_up_sync(0xffffffffu, ipc, o),
+                nt = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) {
+        ic += nc;
+        ipc += npc;
+        it += nt;
+      }
+    }
+    if (e < E) {
+      const int off = base_c + ic - c, poff = base_pc + ipc - pc;
+      counts[e] = c;
+      offsets[e] = off;
+      pad_offsets[e] = poff;
+      s_off[e] = off;
+      s_poff[e] = poff;
+      if (c > 0) touched[base_t + it - 1] = e;
+    }
+    base_c += __shfl_sync(0xffffffffu, ic, 31);
+    base_pc += __shfl_sync(0xffffffffu, ipc, 31);
+    base_t += __shfl_sync(0xffffffffu, it, 31);
+  }
+  if (lane == 0) {
+    offsets[E] = base_c;
+    pad_offsets[E] = base_pc;
+    touched[E] = base_t;
+  }
+  int r = 0;
+  for (int q = 0; q < npairs; ++q) {
+    const int eq = __shfl_sync(0xffffffffu, ep, q);
+    r += (q < lane && eq == ep) ? 1 : 0;
+  }
+  __syncwarp();  // s_off, s_poff of every expert written
+  if (lane < npairs) {
+    const int pos = s_off[ep] + r, ppos = s_poff[ep] + r * rpp;
+    perm_tok[pos] = lane / k;
+    perm_slot[pos] = lane % k;
+    inv[lane] = pos;
+    pad_inv[lane] = ppos;
+    for (int q = 0; q < rpp; ++q) pad_pair[ppos + q] = lane;
+    s_prow[lane] = ppos;
+  }
+}
+
+// Few-token routing in one block of 1024 threads (T <= kSmallRouteT): warps
+// 0..T-1 take the top-k of one token each and warp 0 then groups the pairs
+// (group_warp).  Meanwhile, when `quant` is set, warps T..31 quantise x to
+// MXFP8 (hi + lo blocks when split == 2) into shared memory and zero out;
+// after one block barrier every thread copies blocks of codes and scales into
+// the routed pairs' rows.  So a decode step needs one launch before its GEMMs,
+// and the routing's serial chain overlaps the quantisation.
 __global__ void __launch_bounds__(1024) route_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx, float* __restrict__ w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ pad_offsets,
@@ -286,93 +358,76 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     int32_t* __restrict__ pad_inv, int32_t* __restrict__ pad_pair, int32_t* __restrict__ touched, int split,
     const __nv_bfloat16* __restrict__ x, int d, uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, int r128,
     float* __restrict__ out, int quant) {
+  // [T][d/32 blocks][split][32] codes, then [T][d/32][split] scale bytes
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  __shared__ int s_prow[kSmallRouteT * kMaxK];
+  __shared__ int s_off[kMaxE], s_poff[kMaxE];
   pdl_wait();
   pdl_launch_dependents();
-  __shared__ int s_idx[kSmallRouteT * kMaxK];
-  __shared__ int s_prow[kSmallRouteT * kMaxK];
-  __shared__ int hist[kMaxE], s_off[kMaxE], s_poff[kMaxE];
-  __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int npairs = T * k;
+  const int nblk = d / 32;
+  uint8_t* s_codes = s_dyn;
+  uint8_t* s_sf = s_dyn + (size_t)T * d * split;
 
-  for (int t = wid; t < T; t += (int)(blockDim.x >> 5))
-    topk_warp(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
-  for (int e = tid; e < kMaxE; e += blockDim.x) hist[e] = 0;
-  __syncthreads();  // the block's global writes above are visible to the block from here
-  for (int p = tid; p < npairs; p += blockDim.x) {
-    const int e = idx[p];
-    s_idx[p] = e;
-    atomicAdd(&hist[e], 1);
-  }
-  __syncthreads();
-
-  // exclusive scans of counts, padded counts and the touched flag (tid = expert)
-  const int c = (tid < E) ? hist[tid] : 0;
-  const int pc = (c * split + kPadRows - 1) / kPadRows * kPadRows;
-  const int inc_c = block_scan_incl(c, warp_tot);
-  const int inc_pc = block_scan_incl(pc, warp_tot);
-  const int inc_t = block_scan_incl(c > 0 ? 1 : 0, warp_tot);
-  if (tid < E) {
-    counts[tid] = c;
-    offsets[tid] = s_off[tid] = inc_c - c;
-    pad_offsets[tid] = s_poff[tid] = inc_pc - pc;
-    if (c > 0) touched[inc_t - 1] = tid;
-    if (tid == E - 1) {
-      offsets[E] = inc_c;
-      pad_offsets[E] = inc_pc;
-      touched[E] = inc_t;
+  if (wid < T) {
+    topk_warp(logits + (size_t)wid * E, E, k, lane, idx + (size_t)wid * k, w + (size_t)wid * k);
+    // every token's selection is in idx before warp 0 reads it
+    if (T > 1) named_bar_sync(1, 32 * T);
+    else __syncwarp();
+    if (wid == 0)
+      group_warp(idx, npairs, E, k, split, lane, counts, offsets, pad_offsets, perm_tok, perm_slot, inv, pad_inv,
+                 pad_pair, touched, s_off, s_poff, s_prow);
+  } else if (quant) {
+    const int nthr = (int)blockDim.x - 32 * T;
+    for (int task = tid - 32 * T; task < T * nblk; task += nthr) {
+      const int t = task / nblk, cb = task % nblk;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d) + 4 * cb;
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(src + q);
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[8 * q + 2 * h] = __uint_as_float(wv[h] << 16);
+          v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+        }
+      }
+      uint32_t hi[8], lo[8];
+      int s_lo = 0;
+      const int s_hi = split == 2 ? mxfp8_split_block(v, hi, lo, s_lo) : mxfp8_block(v, hi);
+      uint4* dst = reinterpret_cast<uint4*>(s_codes + (size_t)task * split * 32);
+      dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      dst[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+      s_sf[task * split] = (uint8_t)(s_hi + 127);
+      if (split == 2) {
+        dst[2] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        dst[3] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        s_sf[task * split + 1] = (uint8_t)(s_lo + 127);
+      }
     }
-  }
-  __syncthreads();
-
-  for (int p = tid; p < npairs; p += blockDim.x) {
-    const int t = p / k, j = p % k, e = s_idx[p];
-    int r = 0;  // earlier tokens that chose e (a token chooses an expert at most once)
-    for (int q = 0; q < t * k; ++q) r += (s_idx[q] == e) ? 1 : 0;
-    const int pos = s_off[e] + r, ppos = s_poff[e] + r * split;
-    perm_tok[pos] = t;
-    perm_slot[pos] = j;
-    inv[p] = pos;
-    pad_inv[p] = ppos;
-    for (int q = 0; q < split; ++q) pad_pair[ppos + q] = p;
-    s_prow[p] = ppos;
+    float4* o4 = reinterpret_cast<float4*>(out);
+    for (int i = tid - 32 * T; i < T * d / 4; i += nthr) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (!quant) return;
   __syncthreads();
 
-  const int nblk = d / 32;
   for (int task = tid; task < npairs * nblk; task += blockDim.x) {
-    const int j = task % k, tb = task / k;
-    const int t = tb / nblk, cb = tb % nblk;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d) + 4 * cb;
-    float v[32];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = __ldg(src + q);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        v[8 * q + 2 * h] = __uint_as_float(wv[h] << 16);
-        v[8 * q + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
-      }
-    }
-    uint32_t hi[8], lo[8];
-    int s_lo = 0;
-    const int s_hi = split == 2 ? mxfp8_split_block(v, hi, lo, s_lo) : mxfp8_block(v, hi);
-    const size_t row = (size_t)s_prow[t * k + j];
+    const int p = task / nblk, cb = task % nblk, tb = (p / k) * nblk + cb;
+    const size_t row = (size_t)s_prow[p];
+    const uint4* src = reinterpret_cast<const uint4*>(s_codes + (size_t)tb * split * 32);
     uint4* dst = reinterpret_cast<uint4*>(xq + row * d + 32 * (size_t)cb);
-    dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    dst[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    xsf[act_sf_index(row, cb, r128)] = (uint8_t)(s_hi + 127);
+    dst[0] = src[0];
+    dst[1] = src[1];
+    xsf[act_sf_index(row, cb, r128)] = s_sf[tb * split];
     if (split == 2) {
       uint4* dlo = reinterpret_cast<uint4*>(xq + (row + 1) * d + 32 * (size_t)cb);
-      dlo[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      dlo[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-      xsf[act_sf_index(row + 1, cb, r128)] = (uint8_t)(s_lo + 127);
+      dlo[0] = src[2];
+      dlo[1] = src[3];
+      xsf[act_sf_index(row + 1, cb, r128)] = s_sf[tb * split + 1];
     }
   }
-  float4* o4 = reinterpret_cast<float4*>(out);
-  for (int i = tid; i < T * d / 4; i += blockDim.x) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 }  // namespace
@@ -397,7 +452,18 @@ cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const
                                bool quant, cudaStream_t st) {
   const int E = L->cfg.n_experts, k = L->cfg.top_k;
   const Scratch& s = L->s;
-  return launch_pdl(route_small_kernel, 1, 1024, 0, st, logits, T, E, k, s.topk_idx, s.topk_w, s.counts, s.offsets,
+  // dynamic shared memory: the MXFP8 codes and scales of the T rows of x
+  // (at most kSmallRouteT x 8192 x 2 split codes + their scales)
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute((const void*)route_small_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSmallRouteT * 8192 * 2 + kSmallRouteT * 256 * 2);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const size_t smem = quant ? (size_t)T * L->cfg.d_model * split + (size_t)T * (L->cfg.d_model / 32) * split : 0;
+  return launch_pdl(route_small_kernel, 1, 1024, smem, st, logits, T, E, k, s.topk_idx, s.topk_w, s.counts, s.offsets,
                     s.pad_offsets, s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, split,
                     static_cast<const __nv_bfloat16*>(x), L->cfg.d_model, s.xq, s.xsf, (int)(s.pad_rows_max / 128),
                     out, quant ? 1 : 0);
