@@ -178,11 +178,19 @@ def barrier(ws):
 
 
 def max_over_ranks(v: float, ws: int) -> float:
+    """The largest of the ranks' values (the slowest rank's step time)."""
     if ws == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(ws: int, tokens_per_rank: int, ms_step_max: float) -> float:
+    """Whole-job tokens/s: every rank runs an independent replica on its own
+    tokens (weak scaling), timed by the slowest rank."""
+    return ws * tokens_per_rank / (ms_step_max * 1e-3)
 
 
 class L2Flush:
@@ -293,7 +301,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms_step = max_over_ranks(res["ms"], ws)
-    value = ws * wl.T / (ms_step * 1e-3)
+    value = job_value(ws, wl.T, ms_step)
 
     # ---- dominant kernel roofline
     kms = res["kernels_ms"]
