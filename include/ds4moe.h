@@ -50,6 +50,10 @@
  *   - Every device pointer must be 16-byte aligned.
  *   - Calls on one layer must not overlap: a layer owns its scratch buffers,
  *     so use it from one stream at a time.
+ *   - One GPU per process: the kernels' launch attributes (dynamic shared
+ *     memory size) and the resident CTA-pair count are set up once per process,
+ *     on the device of the first layer that runs them; layers on a second
+ *     device in the same process are not supported.
  *   - NaN or infinite logits or activations are outside the layer's domain
  *     (the output is then unspecified but the call is memory-safe).
  */
