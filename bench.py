@@ -143,9 +143,16 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarize(self.lines)
+
+    @staticmethod
+    def summarize(lines) -> dict:
+        """Median SM clock of the loaded samples (above half the highest), the
+        highest max clock, and the throttle reasons seen active in any sample,
+        from `nvidia-smi --format=csv,noheader,nounits` lines of FIELDS."""
         sms, maxs, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
