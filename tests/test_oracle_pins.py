@@ -305,3 +305,73 @@ def test_tiny_workload_has_no_ties_and_distinct_experts(oracle_lib):
         assert len(set(lg[t].tolist())) == wl.E
     idx, w = oracle_lib.route(lg, wl.k)
     assert np.allclose(w.sum(1), 1.0, atol=1e-15)
+
+
+# ----------------------------------------------------------------- fp16 and the Q2_K super-block stride
+def test_half_golden(oracle_lib):
+    g = GOLDEN["half"]
+    for b, v in zip(g["bits"], g["values"]):
+        got = oracle_lib.half(b)
+        assert got == v and math.copysign(1, got) == math.copysign(1, v), (hex(b), got, v)
+
+
+def test_half_against_numpy_every_pattern(oracle_lib):
+    # every finite binary16 pattern against numpy's float16 (a library routine)
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    for b in range(65536):
+        r = float(ref[b])
+        if math.isnan(r):
+            assert math.isnan(oracle_lib.half(b))
+        else:
+            assert oracle_lib.half(b) == r, hex(b)
+
+
+def _two_superblock_down(g, d):
+    """Q2_K down weights [1][d][2][84] holding the hand-built rows of the pin
+    (rows beyond them are all-zero blocks)."""
+    dq = np.zeros((1, d, 2, 84), np.uint8)
+    for r, row in enumerate(g["rows"]):
+        for sb, blk in enumerate(row):
+            dq[0, r, sb, 0:16] = blk["scale_bytes"]
+            dq[0, r, sb, 16:80] = blk["qs_byte"]
+            dq[0, r, sb, 80:82] = np.array([blk["d_bits"]], np.uint16).view(np.uint8)
+            dq[0, r, sb, 82:84] = np.array([blk["dmin_bits"]], np.uint16).view(np.uint8)
+    return dq
+
+
+def test_q2k_two_superblocks_dequant(oracle_lib):
+    """Weights at super-block index 1 of a 512-weight row (byte 84 of the row)
+    and the row stride of 168 bytes, on hand-worked values."""
+    g = GOLDEN["q2k_two_superblocks"]
+    d, f = 32, 512
+    W = _const_layer(d, f, 1, 0x22, 0x11, 0x22)
+    del W["down_codes"], W["down_scales"]
+    W["down_q2k"] = _two_superblock_down(g, d)
+    _, _, wd = oracle_lib.dequant_expert(_dims(d, 1, f, 1), W, 0)
+    for key, v in g["weights"].items():
+        r, c = (int(s) for s in key.split(","))
+        assert wd[r, c] == v, (key, wd[r, c], v)
+    for r, s in enumerate(g["row_sums"]):
+        assert wd[r].sum() == s
+    assert not wd[len(g["rows"]):].any()
+
+
+@pytest.mark.parametrize("mode", ["exact", "q2k_prefill"])
+def test_q2k_two_superblocks_forward_closed_form(oracle_lib, mode):
+    """The routed forward through the Q2_K row dot: gate = 1.0, up = 0.5 and
+    x = 1 give g = 32, u = 16 and the same h for every feature, so
+    y_m = h * (sum of row m's 512 weights), the hand-worked row sums."""
+    import oracle
+    g = GOLDEN["q2k_two_superblocks"]
+    d, f = 32, 512
+    W = _const_layer(d, f, 1, 0x22, 0x11, 0x22)
+    del W["down_codes"], W["down_scales"]
+    W["down_q2k"] = _two_superblock_down(g, d)
+    x = torch.ones(1, d, dtype=torch.bfloat16)
+    act = oracle.ACT_EXACT if mode == "exact" else oracle.ACT_MXFP8_X_ONLY
+    out = oracle_lib.forward(_dims(d, 1, f, 1), W, _bits(x), np.zeros((1, 1), np.int32), np.ones((1, 1)), [0], act)
+    h = 32.0 / (1.0 + math.exp(-32.0)) * 16.0
+    want = np.zeros(d)
+    want[:len(g["row_sums"])] = [h * s for s in g["row_sums"]]
+    assert np.allclose(out[0], want, rtol=1e-14, atol=0)
