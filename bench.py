@@ -51,10 +51,13 @@ def q2k_bytes(rows: int, K: int) -> int:
 def workload_accounting(wl: synth.Workload, counts: np.ndarray) -> dict:
     """Algorithmic bytes and flops of one forward, per kernel and in total.
 
-    Weights are read once per touched expert (U = experts with >= 1 token);
-    activations: x read once (bf16), logits read once, out written once
-    (fp32); the prefill GEMMs also move their MXFP8 operands once (x_hat per
-    routed pair is an implementation buffer, counted separately)."""
+    Algorithmic bytes are what the layer must move: the weights of every
+    touched expert once (U = experts with >= 1 token), x read once (bf16), the
+    logits read once and out written once (fp32).  Per kernel: gate/up = its
+    weights + x, down = its weights + out.  The MXFP8 (or fp16) activation
+    rows that the grouped GEMMs exchange through HBM (x^ per routed pair, h)
+    belong to this implementation, not to the layer, and are reported apart as
+    implementation bytes."""
     T, d, f, k, E = wl.T, wl.d, wl.f, wl.k, wl.E
     U = int((counts > 0).sum())
     pairs = T * k
@@ -69,31 +72,42 @@ def workload_accounting(wl: synth.Workload, counts: np.ndarray) -> dict:
         "weights_down": dn_w,
         "io": io,
         "total_bytes": gu_w + dn_w + io,
-        # per-kernel algorithmic bytes: weights + the kernel's own activations in/out
-        "gemm_gateup_bytes": gu_w + pairs * d * 33 // 32 + pairs * f * 33 // 32,
-        "gemm_down_bytes": dn_w + pairs * f * 33 // 32 + T * d * 4,
-        "decode_gateup_bytes": gu_w + T * d * 2 + pairs * f * 4,
-        "decode_down_bytes": dn_w + pairs * f * 4 + T * d * 4,
+        # per-kernel algorithmic bytes: the kernel's weights + the layer input or output it touches
+        "gemm_gateup_bytes": gu_w + T * d * 2,
+        "gemm_down_bytes": dn_w + T * d * 4,
+        "decode_gateup_bytes": gu_w + T * d * 2,
+        "decode_down_bytes": dn_w + T * d * 4,
+        # activation rows exchanged through HBM by this implementation (prefill path)
+        "implementation_bytes": {
+            "gemm_gateup": pairs * d * 33 // 32 + (pairs * f * 2 if wl.down == "q2k" else pairs * f * 33 // 32),
+            "gemm_down": pairs * f * 2 if wl.down == "q2k" else pairs * f * 33 // 32,
+        },
         "flops_gateup": flops_gu,
         "flops_down": flops_dn,
         "flops": flops_gu + flops_dn,
     }
 
 
-def measured_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel source changed since those counters were taken."""
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    committed ncu record (profiles/dram_traffic.json), or None when there is no
+    record or the kernel's source file changed since the counters were taken."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as fh:
-            rec = json.load(fh)
-        src = os.path.join(ROOT, "quantized_moe_expert_top_gb300", "csrc", "gemm_pair.cu")
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if sha != rec.get("gemm_pair_cu_sha256_16"):
-            return None
-        return rec.get(kernel)
-    except (OSError, ValueError):
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as fh:
+            recs = json.load(fh)["records"]
+    except (OSError, ValueError, KeyError):
         return None
+    for r in recs:
+        if r.get("kernel") != kernel or r.get("workload") != workload:
+            continue
+        try:
+            src = os.path.join(ROOT, r["source"])
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        except (OSError, KeyError):
+            return None
+        return r.get("bytes_per_launch") if sha == r.get("source_sha256_16") else None
+    return None
 
 
 def load_peaks() -> dict:
@@ -276,6 +290,13 @@ def measure_workload(ds4, layer, wl, steps, warmup, peaks, flush, want_kernels=T
     return res, acc, x, logits, out
 
 
+def config_of(wl: synth.Workload, ws: int) -> dict:
+    """The `config` object of the JSON line (both arms)."""
+    return {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} f={wl.f} top_k={wl.k} down={wl.down}",
+            "T": wl.T, "d": wl.d, "E": wl.E, "f": wl.f, "top_k": wl.k, "routing": wl.routing,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -330,7 +351,8 @@ def run_ours(args):
             roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"]}
         roofline.update({"kernel": dom, "kernel_ms": kms[dom],
-                         "traffic": measured_traffic(dom) if wl.name == "prefill" else None,
+                         "traffic": measured_traffic(dom, wl.name),
+                         "implementation_bytes": acc["implementation_bytes"].get(dom),
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                          else "fallback",
                          "algorithmic_bytes": acc[bytes_key[dom]], "algorithmic_flops": acc[flops_key[dom]]})
@@ -361,21 +383,6 @@ def run_ours(args):
     # ---- the other workloads, same GPU (rank 0 reports them)
     also = {}
     if not args.no_extra:
-        gemv = None
-        if layer_wl.down != "q2k":  # the CUDA-core GEMV decode path, for comparison
-            Wg = synth.make_layer_weights(layer_wl, device="cuda")
-            gemv = ds4.Layer(layer_wl.d, layer_wl.E, layer_wl.f, layer_wl.k, 64, Wg, force_path="decode")
-            del Wg
-            torch.cuda.empty_cache()
-            for name in ("decode1", "decode64"):
-                other = synth.WORKLOADS[name]
-                try:
-                    r, a, *_ = measure_workload(ds4, gemv, other, min(args.steps, 20), args.warmup, peaks, L2Flush())
-                    also[name + "_gemv_path"] = dict(r, algorithmic_bytes=a["total_bytes"])
-                except Exception as exc:
-                    also[name + "_gemv_path"] = {"error": str(exc)}
-            gemv.close()
-            torch.cuda.empty_cache()
         for name in ("decode1", "decode64", "prefill", "q2k"):
             if name == wl.name:
                 continue
@@ -418,9 +425,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "mxfp4(e2m1) x mxfp8(e4m3) -> fp32" if wl.T > 64 else "mxfp4(e2m1) x f16 -> fp32",
         "data": "synthetic (seeded; random-init MXFP4 weights, N(0,1) activations and logits)",
-        "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} f={wl.f} top_k={wl.k} "
-                               f"down={wl.down}", "T": wl.T, "d": wl.d, "E": wl.E, "f": wl.f, "top_k": wl.k,
-                   "routing": wl.routing, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        "config": {**config_of(wl, ws),
                    "l2": ("inputs larger than L2: %.2f GB of expert weights per step" %
                           ((acc["weights_gateup"] + acc["weights_down"]) / 1e9)) if flush is None
                    else "flushed (512 MB write + read back) before every step",
@@ -433,7 +438,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": res["launches"] * (args.steps + min(args.steps, 20)),
+        "gpu_launches": res["launches"] * args.steps,
         "clocks": clk,
         "workloads": also,
         "peaks": peaks,
@@ -501,12 +506,15 @@ def run_reference(args):
     value = toks / secs
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.T / value,
+        "steps": args.steps, "warmup": args.warmup,
+        # a step is a bounded sample of the workload's tokens: this is the measured wall time of one
+        "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} f={wl.f} top_k={wl.k} down={wl.down}"},
+        "config": config_of(wl, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{toks} random tokens over {args.steps} steps ({secs:.1f} s)"},
+                         "sample": f"{toks} random tokens of the {wl.name} workload over {args.steps} steps "
+                                   f"({secs:.1f} s; each step a bounded sample, not the whole {wl.T}-token batch)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

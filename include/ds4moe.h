@@ -54,6 +54,9 @@
  *     memory size) and the resident CTA-pair count are set up once per process,
  *     on the device of the first layer that runs them; layers on a second
  *     device in the same process are not supported.
+ *   - Host threads: that one-time set-up is thread-safe, so different layers
+ *     may be driven from different host threads at the same time; one layer
+ *     is driven by one thread at a time (its last-call state is not locked). 
  *   - NaN or infinite logits or activations are outside the layer's domain
  *     (the output is then unspecified but the call is memory-safe).
  */
@@ -96,10 +99,11 @@ enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2, DS
  *                    MXFP4 only; forcing one of them is then UNSUPPORTED).
  *   decode_max_tokens  AUTO path choice: T <= this runs DECODE_MMA (default 64).
  *   force_path       DS4MOE_PATH_* (AUTO by default; tests force a path).
- *   debug_fault      0 in production.  1 = the first prefill GEMM drops one
- *                    of its operand loads and its waits give up after ~1 ms,
- *                    so ds4moe_get_status() reports DS4MOE_ERR_DEVICE_TIMEOUT
- *                    (fault-handling test; the GPU stays usable).
+ *   debug_fault      0 in production.  1 = in the gate/up GEMM, the first
+ *                    CTA pair's MMA issuer waits on a barrier that nothing
+ *                    arrives on, and the GEMM's waits give up after ~1 ms, so
+ *                    ds4moe_get_status() reports DS4MOE_ERR_DEVICE_TIMEOUT
+ *                    (fault-handling test; no fault, the GPU stays usable).
  *   wait_timeout_ms  bound on every device-side wait (default 2000). */
 typedef struct {
     int32_t d_model, n_experts, d_ff, top_k;
@@ -141,7 +145,7 @@ int ds4moe_layer_create(const ds4moe_config *cfg, const ds4moe_weights *weights,
  *   out     device, fp32 [T][d]; fully overwritten
  *   T       0..max_tokens (T = 0 enqueues nothing)
  * x, logits and out stay owned by the caller and must stay valid until the
- * stream work completes; out must not alias x or logits.
+ * stream work completes; out must not overlap x or logits (INVALID_ARG).
  * Errors (checked on the host before anything is enqueued): INVALID_ARG,
  * TOO_MANY_TOKENS, CUDA (a launch failed).  Device-side timeouts surface
  * later through ds4moe_get_status. */
@@ -165,6 +169,23 @@ int ds4moe_forward_host(ds4moe_layer *layer, const void *x, const float *logits,
  * Errors: INVALID_ARG (no forward yet), CUDA. */
 int ds4moe_get_routing(ds4moe_layer *layer, int32_t *topk_idx, float *topk_w, int32_t *offsets,
                        int32_t *perm_tok, ds4moe_stream_t stream);
+
+/* Diagnostics (the pages have no counterpart): copies out the MXFP8
+ * activation rows that the most recent forward fed to its grouped tensor-core
+ * GEMMs, so that a test can compare these bytes with an independent
+ * quantiser.  Enqueued on `stream` (use the forward's stream).
+ *   which   0 = x (MXFP8 along d, K = d), 1 = h = SwiGLU output (MXFP8
+ *           along f, K = f; MXFP4 down projection only)
+ *   codes   device uint8 [T*k*S][K]   E4M3 codes, 16-byte aligned
+ *   scales  device uint8 [T*k*S][K/32] E8M0 scale bytes
+ * Rows are in token order of the routed pairs, p = t*k + j (j = slot of the
+ * token's top-k), and S rows per pair: S = 1 on the PREFILL path; S = 2 on
+ * DECODE_MMA (row 2p = hi = MXFP8(v), row 2p + 1 = lo = MXFP8(v - hi)).
+ * Returns S (1 or 2) on success, or INVALID_ARG (no forward yet, bad
+ * pointer or `which`), UNSUPPORTED (the last forward ran the DECODE GEMV
+ * path, or which = 1 on a Q2_K layer, whose h stays fp16), CUDA. */
+int ds4moe_get_act_codes(ds4moe_layer *layer, int32_t which, uint8_t *codes, uint8_t *scales,
+                         ds4moe_stream_t stream);
 
 /* Synchronises the stream of the most recent forward, reads and clears the
  * layer's device status word.  Returns DS4MOE_OK, DS4MOE_ERR_DEVICE_TIMEOUT
@@ -205,11 +226,16 @@ const char *ds4moe_kernel_name(const ds4moe_layer *layer, int32_t T, int i);
  *   topk_idx  device int32 [T][k] out, topk_w device fp32 [T][k] out
  *   offsets   device int32 [E+1] out, perm_tok device int32 [T*k] out
  * Results equal those of ds4moe_forward's routing (see ds4moe_get_routing).
+ * T = 0 writes offsets[0..E] = 0 and nothing else (the other pointers may
+ * then be NULL).
  * Enqueued on `stream`; no host synchronisation.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current: make that first call before any stream capture.  Every call shares
- * the one array and nothing in it needs to start at zero; calls whose GPU
- * work overlaps (two streams, two host threads) race on it, so serialise them.
+ * current and keeps it for the rest of the process: make that first call
+ * before any stream capture, and make no call after cudaDeviceReset() on that
+ * device (the kept address belongs to the destroyed context).  Every call
+ * shares the one array and nothing in it needs to start at zero; calls whose
+ * GPU work overlaps (two streams, two host threads) race on it, so serialise
+ * them.
  * Errors: INVALID_ARG (NULL or misaligned pointer, E or k out of range),
  * TOO_MANY_TOKENS (T*k > 16384), CUDA. */
 int ds4moe_route_noalloc(const float *logits, int32_t T, int32_t E, int32_t k, int32_t *topk_idx,

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         L.ds4moe_kernel_name.restype = ctypes.c_char_p
         L.ds4moe_kernel_name.argtypes = [vp, i32, ctypes.c_int]
+        L.ds4moe_get_act_codes.restype = ctypes.c_int
+        L.ds4moe_get_act_codes.argtypes = [vp, i32, vp, vp, vp]
         L.ds4moe_route_noalloc.restype = ctypes.c_int
         L.ds4moe_route_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.ds4moe_status_string.restype = ctypes.c_char_p
@@ -124,15 +126,15 @@ def route_noalloc(logits: torch.Tensor, k: int, stream=None) -> dict:
     library; the output tensors are allocated here by torch)."""
     T, E = logits.shape
     dev = logits.device
-    r = {"topk_idx": torch.empty(T, k, dtype=torch.int32, device=dev),
-         "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
+    r = {"topk_idx": torch.empty(max(T, 1), k, dtype=torch.int32, device=dev),
+         "topk_w": torch.empty(max(T, 1), k, dtype=torch.float32, device=dev),
          "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
          "perm_tok": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)}
     rc = lib().ds4moe_route_noalloc(_ptr(logits), T, E, k, _ptr(r["topk_idx"]), _ptr(r["topk_w"]),
                                     _ptr(r["offsets"]), _ptr(r["perm_tok"]), _stream_handle(stream))
     if rc != OK:
         raise Ds4moeError(rc, "ds4moe_route_noalloc")
-    r["perm_tok"] = r["perm_tok"][:T * k]
+    r["topk_idx"], r["topk_w"], r["perm_tok"] = r["topk_idx"][:T], r["topk_w"][:T], r["perm_tok"][:T * k]
     return r
 
 
@@ -222,6 +224,21 @@ class Layer:
         if rc != OK:
             raise Ds4moeError(rc, "ds4moe_get_routing")
         return r
+
+    def act_codes(self, which: str = "x", stream=None) -> dict:
+        """MXFP8 activation rows of the last forward (diagnostics): x or h
+        codes [T*k*S, K] and scale bytes [T*k*S, K/32] in token order of the
+        routed pairs, S rows per pair (1 on PREFILL, 2 = hi, lo on DECODE_MMA)."""
+        T, k = self._last_T, self.cfg.top_k
+        K = self.cfg.d_model if which == "x" else self.cfg.d_ff
+        dev = torch.device("cuda", torch.cuda.current_device())
+        codes = torch.empty(max(2 * T * k, 1), K, dtype=torch.uint8, device=dev)
+        scales = torch.empty(max(2 * T * k, 1), K // 32, dtype=torch.uint8, device=dev)
+        n = lib().ds4moe_get_act_codes(self._h, 0 if which == "x" else 1, _ptr(codes), _ptr(scales),
+                                       _stream_handle(stream))
+        if n < 0:
+            raise Ds4moeError(n, "ds4moe_get_act_codes")
+        return {"split": n, "codes": codes[:T * k * n], "scales": scales[:T * k * n]}
 
     def status(self) -> int:
         return lib().ds4moe_get_status(self._h)

@@ -97,6 +97,11 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
 // 2^e as f32 for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 
+// 2^e as f32 for every E8M0 exponent e in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float exp2i_e8m0(int e) {
+  return __int_as_float(e > -127 ? (e + 127) << 23 : 0x00400000);
+}
+
 // floor(log2(a)) for finite a > 0 (subnormals clamp to -127).
 __device__ __forceinline__ int floor_log2_f32(float a) {
   int ex = (__float_as_int(a) >> 23) & 0xFF;

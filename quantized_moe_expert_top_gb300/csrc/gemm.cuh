@@ -54,7 +54,7 @@ __device__ __forceinline__ int mxfp8_block(const float (&v)[32], uint32_t (&pack
 // residual.
 __device__ __forceinline__ int mxfp8_split_block(float (&v)[32], uint32_t (&hi)[8], uint32_t (&lo)[8], int& s_lo) {
   const int s = mxfp8_block(v, hi);
-  const float sc = exp2i(s);
+  const float sc = exp2i_e8m0(s);  // s = -127 for a block of subnormals
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float2 a = e4m3x2_to_f32x2(hi[i] & 0xFFFFu), b = e4m3x2_to_f32x2(hi[i] >> 16);

@@ -192,7 +192,7 @@ __device__ __forceinline__ void gateup_slice(const uint32_t (&r)[16], bool gate,
     for (int jj = 0; jj < kHalf; ++jj) {
       s[jj] = mxfp8_exponent(__uint_as_float(am[jj]));
       chi[jj] = f32x2_to_e4m3x2(h[jj] * exp2i(-s[jj]), 0.f) & 0xFFu;
-      res[jj] = h[jj] - e4m3x2_to_f32x2(chi[jj]).x * exp2i(s[jj]);
+      res[jj] = h[jj] - e4m3x2_to_f32x2(chi[jj]).x * exp2i_e8m0(s[jj]);
       am2[jj] = __float_as_uint(fabsf(res[jj]));
     }
     block_amax(am2);
@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
   uint64_t* acc_full = empty + kPBars;                                // [2] accumulator ready
   uint64_t* acc_empty = acc_full + 2;                                 // [2] leader: both epilogues drained it
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* never = drain + 1;                                        // fault test: nothing arrives on it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_ok = abort_flag + 1;
 
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       mbar_init(&acc_empty[b], 2 * kPEpiWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_a);
@@ -308,7 +310,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       int bar = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
-      bool fault_pending = args.debug_fault && blockIdx.x == 0;
       bool ok = true;
       int sfg = 0;  // scale-factor groups issued
       for (bool more = it.first_chunk(); more && ok; more = it.next()) {
@@ -333,12 +334,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
           if (leader) mbar_arrive_expect_tx(&full[bar], stage_bytes * nst + (sf_load ? kSfBytes : 0u));
           for (int i = 0; i < nst; ++i) {
             uint8_t* st = smem + (2 * bar + i) * S::kStage;
-            if (fault_pending) {
-              fault_pending = false;  // test-only: drop this stage's operand loads
-            } else {
-              tma_load_2d_pair(st + S::kA, tb, b_cl, (kb + i) * 128, brow);
-              tma_load_2d_pair(st, &tm_a, b_cl, (kb + i) * 128, tile * 128);
-            }
+            tma_load_2d_pair(st + S::kA, tb, b_cl, (kb + i) * 128, brow);
+            tma_load_2d_pair(st, &tm_a, b_cl, (kb + i) * 128, tile * 128);
           }
           if (sf_load) {
             uint8_t* sf = smem + S::kSfOff + (sfg % kSfRing) * S::kSfGroupBytes;
@@ -354,12 +351,14 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
           }
         }
       }
-      if (*abort_flag && leader) {
-        // every issued step's copies land before the pair exits
+      if (leader) {
+        // The last issued step of every slot has landed (both CTAs' bytes)
+        // before the pair exits: in a normal run these copies are consumed
+        // anyway; after a wait ran out, this is the drain of what is in flight.
         for (int b = 0; b < kPBars; ++b)
           if ((issued_mask >> b) & 1u) {
-            volatile int never = 0;
-            mbar_wait_bounded(&full[b], (issued_parity >> b) & 1u, args.budget_ns, &never);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(&full[b], (issued_parity >> b) & 1u, args.budget_ns, &no_abort);
           }
       }
     }
@@ -380,7 +379,19 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       const uint64_t sfdesc0 = smem_desc(st0 + S::kSfOff, 0, 128, 0);
       static_assert(S::kXchg < (1 << 18), "descriptor address field");
       constexpr uint32_t kSfIdStep = (1u << 4) | (1u << 29);  // next byte of the 32-bit scale word, A and B
-      for (bool more = it.first_chunk(); more && ok; more = it.next(), ++chunk) {
+      if (args.debug_fault && blockIdx.x == 0) {
+        // Fault test: before its first MMA, the first pair's issuer waits on a
+        // barrier that nothing arrives on, so the wait runs out.  Every TMA
+        // load of both CTAs is still issued normally (at most kPBars steps,
+        // since no slot is ever freed), and the producer's drain below waits
+        // for all of them on this CTA's full barriers before the pair exits.
+        if (!mbar_wait_bounded(never, 0, args.budget_ns, abort_flag)) {
+          report_timeout(args.status, kWhereMmaFull);
+          *abort_flag = 1;
+          ok = false;
+        }
+      }
+      for (bool more = ok && it.first_chunk(); more && ok; more = it.next(), ++chunk) {
         const int N = round32(it.nch);
         const int nsf = N > 128 ? 2 : 1;
         const int buf = chunk & 1;
@@ -543,8 +554,9 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
 // this shared memory), asked once.
 template <PMode M>
 int max_pairs(int num_sms) {
-  static int cached = 0;
-  if (cached > 0) return cached;
+  static std::atomic<int> cached{0};
+  const int c = cached.load(std::memory_order_relaxed);
+  if (c > 0) return c;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(num_sms & ~1));
   cfg.blockDim = dim3(kPThreads);
@@ -561,7 +573,7 @@ int max_pairs(int num_sms) {
     cudaGetLastError();
     n = num_sms / 2;
   }
-  cached = n;
+  cached.store(n, std::memory_order_relaxed);  // every thread computes the same value
   return n;
 }
 
@@ -570,13 +582,12 @@ cudaError_t launch_pair(const ds4moe_layer* L, const CUtensorMap& a, const CUten
                         const CUtensorMap* b, const PairArgs& args, cudaStream_t st) {
   BoxMaps maps;
   for (int i = 0; i < kNumBoxMaps; ++i) maps.m[i] = b[i];
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute((const void*)pair_gemm_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PSmem::kTotal);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static InitOnce attr_once;
+  cudaError_t e = init_once(attr_once, [] {
+    return cudaFuncSetAttribute((const void*)pair_gemm_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                PSmem::kTotal);
+  });
+  if (e != cudaSuccess) return e;
   const int per_e = M == PMode::GateUp ? args.rows_per_expert / 128 : (args.rows_per_expert + 255) / 256;
   const int units = args.E * per_e;
   const int mp = max_pairs<M>(L->num_sms);

@@ -6,11 +6,31 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/ds4moe.h"
 
 namespace ds4moe {
 
 struct DeviceStatus;
+
+// Process-wide launch set-up (a kernel's dynamic shared-memory limit, the
+// resident CTA-pair count) done once, safely when several host threads launch
+// at the same time; a failed attempt is retried by the next call.
+struct InitOnce {
+  std::atomic<bool> done{false};
+  std::mutex mu;
+};
+template <typename F>
+inline cudaError_t init_once(InitOnce& o, F&& f) {
+  if (o.done.load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(o.mu);
+  if (o.done.load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = f();
+  if (e == cudaSuccess) o.done.store(true, std::memory_order_release);
+  return e;
+}
 
 // Launches `kernel` on `st` with programmatic stream serialisation, so that
 // its blocks can be scheduled while the previous kernel in the stream drains
@@ -110,6 +130,8 @@ struct ds4moe_layer {
   bool timing;
   int last_nk;         // kernels in the most recent forward
   int last_T;
+  int last_path;       // DS4MOE_PATH_* of the most recent forward
+  int last_split;      // activation rows per routed pair in that forward (1 or 2)
   cudaStream_t last_stream;
   bool has_forward;
   bool prefill_ready;  // tensor maps encoded
@@ -138,6 +160,10 @@ cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, i
 cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+// Diagnostics: the `split` MXFP8 rows of every routed pair (token order) of
+// the x (which = 0) or h (which = 1) activations of the last forward.
+cudaError_t launch_gather_act(const ds4moe_layer* L, int which, int T, int split, uint8_t* codes, uint8_t* scales,
+                              cudaStream_t st);
 
 // create-time repacking
 cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int tile_rows, int row_off,

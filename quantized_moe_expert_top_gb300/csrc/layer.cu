@@ -103,15 +103,18 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 PFN_encodeTiled get_encode_fn() {
-  static PFN_encodeTiled fn = nullptr;
-  if (!fn) {
+  static std::atomic<PFN_encodeTiled> fn{nullptr};
+  PFN_encodeTiled f = fn.load(std::memory_order_acquire);
+  if (!f) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_encodeTiled)p;
+        q == cudaDriverEntryPointSuccess) {
+      f = (PFN_encodeTiled)p;
+      fn.store(f, std::memory_order_release);  // every thread finds the same entry point
+    }
   }
-  return fn;
+  return f;
 }
 
 // 2-D row-major tensor map: inner dimension `inner` elements, `rows` rows,
@@ -438,6 +441,14 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   if (T > L->cfg.max_tokens) return DS4MOE_ERR_TOO_MANY_TOKENS;
   if (T == 0) return DS4MOE_OK;
   if (!x || !logits || !out || !aligned16(x) || !aligned16(logits) || !aligned16(out)) return DS4MOE_ERR_INVALID_ARG;
+  {
+    // out may not overlap x or logits (the kernels zero and accumulate into out
+    // while x and the logits are still being read)
+    const uintptr_t o0 = (uintptr_t)out, o1 = o0 + (uintptr_t)T * L->cfg.d_model * 4;
+    const uintptr_t x0 = (uintptr_t)x, x1 = x0 + (uintptr_t)T * L->cfg.d_model * 2;
+    const uintptr_t l0 = (uintptr_t)logits, l1 = l0 + (uintptr_t)T * L->cfg.n_experts * 4;
+    if ((o0 < x1 && x0 < o1) || (o0 < l1 && l0 < o1)) return DS4MOE_ERR_INVALID_ARG;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int path = path_of(L, T);
   if (path == DS4MOE_PATH_DECODE && !L->s.h_dec) return DS4MOE_ERR_UNSUPPORTED;
@@ -484,6 +495,8 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
     return DS4MOE_ERR_CUDA;
   }
   L->last_T = T;
+  L->last_path = path;
+  L->last_split = split;
   L->has_forward = true;
   return DS4MOE_OK;
 }
@@ -529,6 +542,21 @@ int ds4moe_get_routing(ds4moe_layer* L, int32_t* topk_idx, float* topk_w, int32_
     return DS4MOE_ERR_CUDA;
   }
   return DS4MOE_OK;
+}
+
+int ds4moe_get_act_codes(ds4moe_layer* L, int32_t which, uint8_t* codes, uint8_t* scales, ds4moe_stream_t stream) {
+  if (!L || !L->has_forward || (which != 0 && which != 1) || !codes || !scales || !aligned16(codes))
+    return DS4MOE_ERR_INVALID_ARG;
+  if (L->last_path == DS4MOE_PATH_DECODE) return DS4MOE_ERR_UNSUPPORTED;         // the GEMV path has no MXFP8 rows
+  if (which == 1 && L->cfg.down_format == DS4MOE_DOWN_Q2K) return DS4MOE_ERR_UNSUPPORTED;  // h stays fp16 there
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != L->device) return DS4MOE_ERR_INVALID_ARG;
+  if (launch_gather_act(L, which, L->last_T, L->last_split, codes, scales,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  return L->last_split;
 }
 
 int ds4moe_get_status(ds4moe_layer* L) {

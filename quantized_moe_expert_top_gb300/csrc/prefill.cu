@@ -485,7 +485,34 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
   }
 }
 
+// --------------------------------------------------------------- diagnostics
+// Copies the `split` activation rows of every routed pair p = t*k + j (token
+// order) out of the expert-grouped padded buffers: codes[(p*split + q)][K] and
+// scales[(p*split + q)][K/32] from padded row pad_inv[p] + q.  One block per
+// output row.
+__global__ void gather_act_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int K, int r128,
+                                  const int32_t* __restrict__ pad_inv, int split, uint8_t* __restrict__ codes,
+                                  uint8_t* __restrict__ scales) {
+  const int orow = blockIdx.x;
+  const size_t src = (size_t)__ldg(pad_inv + orow / split) + (size_t)(orow % split);
+  const uint4* s4 = reinterpret_cast<const uint4*>(q + src * K);
+  uint4* d4 = reinterpret_cast<uint4*>(codes + (size_t)orow * K);
+  for (int i = threadIdx.x; i < K / 16; i += blockDim.x) d4[i] = s4[i];
+  for (int b = threadIdx.x; b < K / 32; b += blockDim.x) scales[(size_t)orow * (K / 32) + b] = sf[act_sf_index(src, b, r128)];
+}
+
 }  // namespace
+
+cudaError_t launch_gather_act(const ds4moe_layer* L, int which, int T, int split, uint8_t* codes, uint8_t* scales,
+                              cudaStream_t st) {
+  const int K = which == 0 ? L->cfg.d_model : L->cfg.d_ff;
+  const uint8_t* q = which == 0 ? L->s.xq : L->s.hq;
+  const uint8_t* sf = which == 0 ? L->s.xsf : L->s.hsf;
+  const int rows = T * L->cfg.top_k * split;
+  gather_act_kernel<<<rows, 128, 0, st>>>(q, sf, K, (int)(L->s.pad_rows_max / 128), L->s.pad_inv, split, codes,
+                                          scales);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, int split, cudaStream_t st) {
   const int parts = (L->cfg.d_model / 32 + 31) / 32;  // warps per token
@@ -496,13 +523,12 @@ cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, i
 
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
   (void)T;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute((const void*)q2k_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         QSmem::kTotal);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static InitOnce attr_once;
+  cudaError_t e = init_once(attr_once, [] {
+    return cudaFuncSetAttribute((const void*)q2k_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                QSmem::kTotal);
+  });
+  if (e != cudaSuccess) return e;
   BoxMaps maps;
   for (int i = 0; i < kNumBoxMaps; ++i) maps.m[i] = L->tm_h16[i];
   Q2kArgs a{};

@@ -454,14 +454,12 @@ cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const
   const Scratch& s = L->s;
   // dynamic shared memory: the MXFP8 codes and scales of the T rows of x
   // (at most kSmallRouteT x 8192 x 2 split codes + their scales)
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute((const void*)route_small_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmallRouteT * 8192 * 2 + kSmallRouteT * 256 * 2);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static InitOnce attr_once;
+  const cudaError_t e = init_once(attr_once, [] {
+    return cudaFuncSetAttribute((const void*)route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmallRouteT * 8192 * 2 + kSmallRouteT * 256 * 2);
+  });
+  if (e != cudaSuccess) return e;
   const size_t smem = quant ? (size_t)T * L->cfg.d_model * split + (size_t)T * (L->cfg.d_model / 32) * split : 0;
   return launch_pdl(route_small_kernel, 1, 1024, smem, st, logits, T, E, k, s.topk_idx, s.topk_w, s.counts, s.offsets,
                     s.pad_offsets, s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, split,
@@ -503,7 +501,16 @@ extern "C" int ds4moe_route_noalloc(const float* logits, int32_t T, int32_t E, i
   auto misaligned = [](const void* p) { return ((uintptr_t)p & 15u) != 0; };
   if (T < 0 || E < 1 || E > kNoAllocMaxE || k < 1 || k > 8 || k > E) return DS4MOE_ERR_INVALID_ARG;
   if ((int64_t)T * k > kNoAllocMaxPairs) return DS4MOE_ERR_TOO_MANY_TOKENS;
-  if (T == 0) return DS4MOE_OK;
+  if (T == 0) {
+    // no pairs: every expert's offset is 0 (the other outputs are empty)
+    if (!offsets || misaligned(offsets)) return DS4MOE_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return DS4MOE_ERR_CUDA;
+    }
+    return DS4MOE_OK;
+  }
   if (!logits || !topk_idx || !topk_w || !offsets || !perm_tok) return DS4MOE_ERR_INVALID_ARG;
   if (misaligned(logits) || misaligned(topk_idx) || misaligned(topk_w) || misaligned(offsets) || misaligned(perm_tok))
     return DS4MOE_ERR_INVALID_ARG;

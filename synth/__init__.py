@@ -88,6 +88,11 @@ WORKLOADS = {
     # expert still receives about 128 tokens (the per-expert GEMM shape of the
     # 4096-token chunk) while the device holds well under 1 GB
     "prefill_e32": Workload("prefill_e32", 512, 4096, 32, 2048, 8, 3, 1, "normal"),
+    # profiling cases of the few-token and Q2_K paths with fewer experts (the
+    # per-expert shapes of the full workloads, a fraction of the device memory)
+    "decode1_e32": Workload("decode1_e32", 1, 4096, 32, 2048, 8, 1, 1, "normal"),
+    "decode64_e64": Workload("decode64_e64", 64, 4096, 64, 2048, 8, 2, 1, "zipf"),
+    "q2k_e64": Workload("q2k_e64", 512, 4096, 64, 2048, 8, 4, 4, "normal", "q2k"),
 }
 
 

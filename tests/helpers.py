@@ -49,18 +49,21 @@ def assert_parity(out_gpu, ref, what=""):
     return m
 
 
-def sample_tokens(idx: np.ndarray, counts: np.ndarray, n: int, seed: int = 0) -> list:
-    """Tokens for sampled parity: first, last, some routed to the most and the
-    least loaded experts, and a seeded random remainder."""
-    T = idx.shape[0]
-    rng = np.random.default_rng(seed)
-    pick = {0, T - 1}
-    order = np.argsort(counts)
-    for e in list(order[-2:]) + [x for x in order if counts[x] > 0][:2]:
-        hits = np.nonzero((idx == e).any(axis=1))[0]
-        if hits.size:
-            pick.add(int(hits[0]))
-            pick.add(int(hits[-1]))
-    while len(pick) < min(n, T):
-        pick.add(int(rng.integers(0, T)))
+def coverage_tokens(idx: np.ndarray, E: int, chunk: int = 128) -> list:
+    """Tokens for sampled parity at full size that reach every expert and both
+    ends of every block of `chunk` consecutive tokens of an expert (the grouped
+    GEMMs split an expert's token columns into chunks that start on 128-token
+    boundaries): for each expert with n routed tokens in (expert, token) order,
+    the tokens at positions 0 and n - 1 and at b - 1 and b for every multiple b
+    of `chunk` below n."""
+    pick = set()
+    for e in range(E):
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        n = toks.size
+        if n == 0:
+            continue
+        pos = {0, n - 1}
+        for b in range(chunk, n, chunk):
+            pos.update((b - 1, b))
+        pick.update(int(toks[p]) for p in pos)
     return sorted(pick)

@@ -43,11 +43,30 @@ def test_traffic_record_counts_only_for_the_profiled_source(tmp_path, monkeypatc
     (tmp_path / "profiles").mkdir()
     (src / "gemm_pair.cu").write_bytes(b"// kernel v1\n")
     sha = hashlib.sha256(b"// kernel v1\n").hexdigest()[:16]
-    (tmp_path / "profiles" / "gemm_traffic.json").write_text(
-        json.dumps({"gemm_pair_cu_sha256_16": sha, "gemm_gateup": 123, "gemm_down": 45}))
+    rel = "quantized_moe_expert_top_gb300/csrc/gemm_pair.cu"
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps({"records": [
+        {"kernel": "gemm_gateup", "workload": "prefill", "source": rel, "source_sha256_16": sha,
+         "bytes_per_launch": 123},
+        {"kernel": "gemm_down", "workload": "prefill", "source": rel, "source_sha256_16": sha,
+         "bytes_per_launch": 45}]}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.measured_traffic("gemm_gateup") == 123
-    assert bench.measured_traffic("gemm_down") == 45
-    assert bench.measured_traffic("act_quant") is None
+    assert bench.measured_traffic("gemm_gateup", "prefill") == 123
+    assert bench.measured_traffic("gemm_down", "prefill") == 45
+    assert bench.measured_traffic("gemm_down", "decode1") is None   # no record for that workload
+    assert bench.measured_traffic("act_quant", "prefill") is None
     (src / "gemm_pair.cu").write_bytes(b"// kernel v2\n")  # changed since the capture
-    assert bench.measured_traffic("gemm_gateup") is None
+    assert bench.measured_traffic("gemm_gateup", "prefill") is None
+
+
+def test_algorithmic_bytes_follow_the_layer_not_the_implementation():
+    import synth
+    wl = synth.WORKLOADS["prefill"]
+    counts = [wl.T * wl.k // wl.E] * wl.E
+    import numpy as np
+    acc = bench.workload_accounting(wl, np.array(counts))
+    # gate/up: 256 experts x 2 x 2048 x 4096 x 17/32 B of weights + x in bf16
+    assert acc["gemm_gateup_bytes"] == 256 * 2 * 2048 * 4096 * 17 // 32 + 4096 * 4096 * 2
+    # down: weights + out in fp32; the MXFP8 rows are implementation bytes
+    assert acc["gemm_down_bytes"] == 256 * 4096 * 2048 * 17 // 32 + 4096 * 4096 * 4
+    assert acc["implementation_bytes"]["gemm_gateup"] == 32768 * (4096 + 2048) * 33 // 32
+    assert acc["total_bytes"] == 3422552064 + 4096 * 4096 * 2 + 4096 * 256 * 4 + 4096 * 4096 * 4

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_parity, bf16_bits, dims_of, host_weights, sample_tokens
+from helpers import assert_parity, bf16_bits, coverage_tokens, dims_of, host_weights
 from test_gpu_b_decode import MID, UNIT, _run
 
 pytestmark = pytest.mark.gpu
@@ -25,7 +25,7 @@ def test_prefill_chunks_past_256_tokens(ds4):
     assert_parity(out, ref, "hot")
 
 
-def test_prefill_4096_tokens_sampled(ds4, big_layer):
+def test_prefill_4096_tokens_every_expert_and_chunk_end(ds4, big_layer):
     wl = synth.WORKLOADS["prefill"]
     layer = big_layer["layer"]
     inp = synth.make_inputs(wl, device="cuda")
@@ -36,7 +36,7 @@ def test_prefill_4096_tokens_sampled(ds4, big_layer):
     out = out.cpu().numpy()
     assert np.isfinite(out).all()
     idx, w = oracle.route(inp["logits"].cpu().numpy(), wl.k)
-    counts = np.bincount(idx.ravel(), minlength=wl.E)
-    toks = sample_tokens(idx, counts, 24, seed=3)
+    toks = coverage_tokens(idx, wl.E)  # every expert, both ends of its 128-token chunks (~340 tokens)
+    assert set(idx[toks].ravel().tolist()) == set(range(wl.E))
     ref = oracle.forward(dims_of(wl), big_layer["Wh"], bf16_bits(inp["x"]), idx, w, toks, oracle.ACT_MXFP8)
     assert_parity(out[toks], ref, "prefill")

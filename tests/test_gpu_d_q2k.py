@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_parity, bf16_bits, dims_of, host_weights, sample_tokens
+from helpers import assert_parity, bf16_bits, coverage_tokens, dims_of, host_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def test_q2k_decode_paths_are_rejected(ds4, path):
     assert ei.value.code == ds4.ERR_UNSUPPORTED
 
 
-def test_q2k_2048_tokens_sampled(ds4):
+def test_q2k_2048_tokens_every_expert_and_chunk_end(ds4):
     wl = synth.WORKLOADS["q2k"]
     W = synth.make_layer_weights(wl, device="cuda")
     torch.cuda.synchronize()
@@ -53,8 +53,8 @@ def test_q2k_2048_tokens_sampled(ds4):
     out = out.cpu().numpy()
     assert np.isfinite(out).all()
     idx, w = oracle.route(inp["logits"].cpu().numpy(), wl.k)
-    counts = np.bincount(idx.ravel(), minlength=wl.E)
-    toks = sample_tokens(idx, counts, 16, seed=4)
+    toks = coverage_tokens(idx, wl.E)  # every expert, both ends of its 128-token chunks (~170 tokens)
+    assert set(idx[toks].ravel().tolist()) == set(range(wl.E))
     ref = oracle.forward(dims_of(wl), Wh, bf16_bits(inp["x"]), idx, w, toks, oracle.ACT_MXFP8_X_ONLY)
     assert_parity(out[toks], ref, "q2k")
     layer.close()

@@ -49,6 +49,22 @@ def test_misaligned_pointer_rejected(ds4, tiny):
     assert ei.value.code == ds4.ERR_INVALID_ARG
 
 
+def test_out_overlapping_an_input_is_rejected(ds4, tiny):
+    wl, _, layer = tiny
+    buf = torch.zeros(4 * wl.d * 4 + 4 * wl.E * 4, dtype=torch.uint8, device="cuda")
+    out = buf[:4 * wl.d * 4].view(torch.float32).view(4, wl.d)
+    x = buf[:4 * wl.d * 2].view(torch.bfloat16).view(4, wl.d)            # x inside out
+    lg = torch.zeros(4, wl.E, dtype=torch.float32, device="cuda")
+    with pytest.raises(ds4.Ds4moeError) as ei:
+        layer.forward(x, lg, out)
+    assert ei.value.code == ds4.ERR_INVALID_ARG
+    x2 = torch.zeros(4, wl.d, dtype=torch.bfloat16, device="cuda")
+    lg2 = buf[4 * wl.d * 4 - 64:4 * wl.d * 4 - 64 + 4 * wl.E * 4].view(torch.float32).view(4, wl.E)  # logits overlap out's tail
+    with pytest.raises(ds4.Ds4moeError) as ei:
+        layer.forward(x2, lg2, out)
+    assert ei.value.code == ds4.ERR_INVALID_ARG
+
+
 def test_path_choice_and_launch_counts(ds4, tiny):
     _, _, layer = tiny
     assert layer.path_for(4) == ds4.PATH_DECODE_MMA

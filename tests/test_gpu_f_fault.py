@@ -1,7 +1,8 @@
-"""Failure detection without a GPU fault: a test-only knob makes one prefill
-GEMM CTA drop one of its operand loads, so its bounded waits run out (~1 ms).
-The kernel records the timeout in the layer's status word and exits cleanly;
-the host reads DS4MOE_ERR_DEVICE_TIMEOUT and the GPU stays usable."""
+"""Failure detection without a GPU fault: a test-only knob makes the first
+CTA pair of the gate/up GEMM wait on a barrier that nothing arrives on, so its
+bounded waits run out (~1 ms).  The kernel records the timeout in the layer's
+status word, lets every copy it issued land and exits cleanly; the host reads
+DS4MOE_ERR_DEVICE_TIMEOUT and the GPU stays usable."""
 import pytest
 import torch
 
@@ -12,7 +13,7 @@ from helpers import assert_parity, bf16_bits, dims_of, host_weights
 pytestmark = pytest.mark.gpu
 
 
-def test_dropped_load_times_out_and_reports(ds4):
+def test_unarrived_barrier_times_out_and_reports(ds4):
     wl = synth.WORKLOADS["tiny"]
     W = synth.make_layer_weights(wl, device="cuda")
     inp = synth.make_inputs(wl, device="cuda")
