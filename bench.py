@@ -335,8 +335,10 @@ def run_ours(args):
     kms = res["kernels_ms"]
     dom = max(kms, key=kms.get) if kms else None
     bytes_key = {"gemm_gateup": "gemm_gateup_bytes", "gemm_down": "gemm_down_bytes",
+                 "decode_mma_gateup": "decode_gateup_bytes", "decode_mma_down": "decode_down_bytes",
                  "decode_gateup": "decode_gateup_bytes", "decode_down": "decode_down_bytes"}
     flops_key = {"gemm_gateup": "flops_gateup", "gemm_down": "flops_down",
+                 "decode_mma_gateup": "flops_gateup", "decode_mma_down": "flops_down",
                  "decode_gateup": "flops_gateup", "decode_down": "flops_down"}
     roofline = None
     if dom in bytes_key:

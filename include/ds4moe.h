@@ -209,8 +209,10 @@ int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
  * error.  ds4moe_kernel_name(layer, T, i) names the i-th kernel a forward of
  * T tokens enqueues (NULL past the end):
  *   DECODE:                route_topk, route_group, decode_gateup, decode_down
- *   other paths, T <= 4:   route_small, gemm_gateup, gemm_down
- *   other paths, T > 4:    route_topk, route_group, act_quant, gemm_gateup, gemm_down */
+ *   DECODE_MMA, T <= 4:    route_small, decode_mma_gateup, decode_mma_down
+ *   DECODE_MMA, T > 4:     route_topk, route_group, act_quant, decode_mma_gateup, decode_mma_down
+ *   PREFILL, T <= 4:       route_small, gemm_gateup, gemm_down
+ *   PREFILL, T > 4:        route_topk, route_group, act_quant, gemm_gateup, gemm_down */
 int ds4moe_set_kernel_timing(ds4moe_layer *layer, int enable);
 int ds4moe_kernel_times(ds4moe_layer *layer, float *ms, int max_n);
 const char *ds4moe_kernel_name(const ds4moe_layer *layer, int32_t T, int i);

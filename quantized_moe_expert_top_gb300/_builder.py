@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libds4moe.so")
-SOURCES = ["layer.cu", "route.cu", "decode.cu", "prefill.cu", "gemm_pair.cu"]
+SOURCES = ["layer.cu", "route.cu", "decode.cu", "prefill.cu", "gemm_pair.cu", "decode_mma.cu"]
 HEADERS = ["common.cuh", "gemm.cuh", "internal.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -83,6 +83,9 @@ struct Scratch {
   uint8_t* hq;           // [pad_rows_max][f]   MXFP8 codes of h (MXFP4 down)
   uint8_t* hsf;          // [f/128][pad_rows_max/128][512]
   __half* h16;           // [pad_rows_max][f]   fp16 h (Q2_K down)
+  float* gu_acc;         // [Tdec*k][2f] DECODE_MMA gate/up partial sums (zero between calls)
+  int32_t* tile_cnt;     // [E][f/64][dec_maxch] K slices done per gate/up tile and token chunk
+  int dec_maxch;         // 128-row token chunks per expert at the DECODE_MMA token limit
   uint8_t* stage_x;      // host-call staging: x [Tmax][d] bf16
   float* stage_logits;   // [Tmax][E]
   float* stage_out;      // [Tmax][d]
@@ -126,6 +129,15 @@ struct ds4moe_layer {
   CUtensorMap tm_xq[ds4moe::kNumBoxMaps];   // 8-bit x, boxes 128 B x (16 * (i + 1)) rows
   CUtensorMap tm_hq[ds4moe::kNumBoxMaps];   // 8-bit h
   CUtensorMap tm_h16[ds4moe::kNumBoxMaps];  // fp16 h, boxes 64 x (16 * (i + 1)) rows
+  // DECODE_MMA (one CTA per SM): 3-D views {128, rows, K/128} that load two
+  // K = 128 blocks per box, and activation scale chunks of one row block
+  CUtensorMap tm_gu3;     // gate/up weights, box 128 x 128 rows x 2
+  CUtensorMap tm_dn3;     // down weights, same
+  CUtensorMap tm_xq3[8];  // x rows, boxes 128 x (16 * (i + 1)) rows x 2
+  CUtensorMap tm_hq3[8];  // h rows, same
+  CUtensorMap tm_sfb_x1;  // x scale chunks: 1 row block x 4 K blocks per box
+  CUtensorMap tm_sfb_h1;  // h scale chunks, same
+  bool decmma_ready;      // the maps above are encoded
   cudaEvent_t ev[8];   // kernel timing events (created when timing is enabled)
   bool timing;
   int last_nk;         // kernels in the most recent forward
@@ -160,6 +172,10 @@ cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, i
 cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+// DECODE_MMA grouped GEMMs (one CTA per SM, split-K over the touched experts'
+// weight tiles); the activation rows are split (hi, lo) as above.
+cudaError_t launch_decmma_gateup(const ds4moe_layer* L, int T, cudaStream_t st);
+cudaError_t launch_decmma_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
 // Diagnostics: the `split` MXFP8 rows of every routed pair (token order) of
 // the x (which = 0) or h (which = 1) activations of the last forward.
 cudaError_t launch_gather_act(const ds4moe_layer* L, int which, int T, int split, uint8_t* codes, uint8_t* scales,

@@ -131,6 +131,22 @@ bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, void* base, uint64_t inn
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view {128 elements, rows, K/128} of a row-major matrix whose rows are
+// `pitch` bytes apart and whose K = 128 blocks are `kstride` bytes apart, with
+// a box of 128 elements x box_rows rows x 2 blocks (128-byte swizzle): one load
+// brings two K = 128 blocks as two consecutive [box_rows][128-byte] tiles.
+bool encode_3d_kblocks(CUtensorMap* tm, CUtensorMapDataType dt, void* base, uint64_t rows, uint64_t kblocks,
+                       uint64_t pitch, uint64_t kstride, uint32_t box_rows) {
+  PFN_encodeTiled fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, rows, kblocks};
+  cuuint64_t strides[2] = {pitch, kstride};
+  cuuint32_t box[3] = {128, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Scale-factor chunk arrays as rows of 256 bytes (two rows per 512-byte
 // chunk), no swizzle.  Weight scales [tiles][K/128][512]: 2-D, box 256 x 8 =
 // the chunks of 4 consecutive K blocks of one tile.  Activation scales
@@ -147,12 +163,12 @@ bool encode_sf_weights(CUtensorMap* tm, void* base, uint64_t chunks) {
             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-bool encode_sf_acts(CUtensorMap* tm, void* base, uint64_t r128, uint64_t kblocks) {
+bool encode_sf_acts(CUtensorMap* tm, void* base, uint64_t r128, uint64_t kblocks, uint32_t row_blocks = 2) {
   PFN_encodeTiled fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {256, r128 * 2, kblocks};
   cuuint64_t strides[2] = {256, r128 * 512};
-  cuuint32_t box[3] = {256, 4, 4};
+  cuuint32_t box[3] = {256, 2 * row_blocks, 4};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -203,12 +219,15 @@ int kernel_list(const ds4moe_layer* L, int T, const char** names) {
   const int path = path_of(L, T);
   if (path == DS4MOE_PATH_DECODE) {
     for (const char* k : {"route_topk", "route_group", "decode_gateup", "decode_down"}) names[n++] = k;
-  } else if (T <= kSmallRouteT) {
-    names[n++] = "route_small";
-    names[n++] = "gemm_gateup";
-    names[n++] = "gemm_down";
   } else {
-    for (const char* k : {"route_topk", "route_group", "act_quant", "gemm_gateup", "gemm_down"}) names[n++] = k;
+    if (T <= kSmallRouteT) {
+      names[n++] = "route_small";
+    } else {
+      for (const char* k : {"route_topk", "route_group", "act_quant"}) names[n++] = k;
+    }
+    const bool dm = path == DS4MOE_PATH_DECODE_MMA;
+    names[n++] = dm ? "decode_mma_gateup" : "gemm_gateup";
+    names[n++] = dm ? "decode_mma_down" : "gemm_down";
   }
   return n;
 }
@@ -324,6 +343,11 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       TRY(alloc(L, &s.xh, (size_t)Tdec * d * 2));
       TRY(alloc(L, &s.xsig, (size_t)Tdec * 4));
     }
+    if (split_ok) {
+      s.dec_maxch = (int)((2 * (int64_t)Tdec + 127) / 128);
+      TRY(alloc(L, &s.gu_acc, (size_t)Tdec * k * 2 * f * 4));
+      TRY(alloc(L, &s.tile_cnt, (size_t)E * (f / 64) * s.dec_maxch * 4));
+    }
     if (need_pre) {
       TRY(alloc(L, &s.xq, (size_t)pad_rows * d));
       TRY(alloc(L, &s.xsf, (size_t)pad_rows * d / 32));
@@ -342,6 +366,10 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
     cudaStream_t st = nullptr;
     bool ok = cudaMemset(L->status, 0, sizeof(DeviceStatus)) == cudaSuccess;
     ok = ok && cudaMemset(s.pad_pair, 0xFF, (size_t)pad_rows * 4) == cudaSuccess;
+    if (split_ok) {
+      ok = ok && cudaMemset(s.gu_acc, 0, (size_t)Tdec * k * 2 * f * 4) == cudaSuccess;
+      ok = ok && cudaMemset(s.tile_cnt, 0, (size_t)E * (f / 64) * s.dec_maxch * 4) == cudaSuccess;
+    }
     if (need_pre) {
       // padding rows of the activation buffers hold zeros (finite codes)
       ok = ok && cudaMemset(s.xq, 0, (size_t)pad_rows * d) == cudaSuccess;
@@ -399,6 +427,22 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
         tm_ok = tm_ok && encode_sf_weights(&L->tm_sfa_dn, w.down_sf, (uint64_t)E * (d / 128) * (f / 128));
         tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h, s.hsf, r128, (uint64_t)f / 128);
       }
+      if (split_ok && !q2k) {
+        tm_ok = tm_ok && encode_3d_kblocks(&L->tm_gu3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu,
+                                           (uint64_t)E * f * 2, (uint64_t)d / 128, w.pitch_gu, 64, 128);
+        tm_ok = tm_ok && encode_3d_kblocks(&L->tm_dn3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn,
+                                           (uint64_t)E * d, (uint64_t)f / 128, w.pitch_dn, 64, 128);
+        for (int b = 0; b < 8; ++b) {
+          const uint32_t rows = 16u * (uint32_t)(b + 1);
+          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_xq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, pad_rows,
+                                             (uint64_t)d / 128, d, 128, rows);
+          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_hq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, pad_rows,
+                                             (uint64_t)f / 128, f, 128, rows);
+        }
+        tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_x1, s.xsf, r128, (uint64_t)d / 128, 1);
+        tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h1, s.hsf, r128, (uint64_t)f / 128, 1);
+        L->decmma_ready = tm_ok;
+      }
       if (!tm_ok) {
         rc = DS4MOE_ERR_CUDA;
         goto fail;
@@ -453,6 +497,7 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   const int path = path_of(L, T);
   if (path == DS4MOE_PATH_DECODE && !L->s.h_dec) return DS4MOE_ERR_UNSUPPORTED;
   if (path != DS4MOE_PATH_DECODE && !L->prefill_ready) return DS4MOE_ERR_UNSUPPORTED;
+  if (path == DS4MOE_PATH_DECODE_MMA && !L->decmma_ready) return DS4MOE_ERR_UNSUPPORTED;
   if (path == DS4MOE_PATH_DECODE_MMA &&
       2 * (int64_t)T * L->cfg.top_k + (int64_t)L->cfg.n_experts * (kPadRows - 1) > L->s.pad_rows_max)
     return DS4MOE_ERR_UNSUPPORTED;
@@ -483,10 +528,15 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
       if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
       if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, split, st));
     }
-    if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, split, st));
-    if (e == cudaSuccess) {
-      if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = mark(launch_gemm_down_q2k(L, out, T, st));
-      else e = mark(launch_gemm_down(L, out, T, split, st));
+    if (path == DS4MOE_PATH_DECODE_MMA) {
+      if (e == cudaSuccess) e = mark(launch_decmma_gateup(L, T, st));
+      if (e == cudaSuccess) e = mark(launch_decmma_down(L, out, T, st));
+    } else {
+      if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, split, st));
+      if (e == cudaSuccess) {
+        if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = mark(launch_gemm_down_q2k(L, out, T, st));
+        else e = mark(launch_gemm_down(L, out, T, split, st));
+      }
     }
   }
   L->last_nk = nk - 1;
@@ -571,6 +621,17 @@ int ds4moe_get_status(ds4moe_layer* L) {
     DeviceStatus z;
     memset(&z, 0, sizeof(z));
     if (cudaMemcpy(L->status, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return DS4MOE_ERR_CUDA;
+    // a call that gave up may have left partial sums and tile counts behind;
+    // the next call expects them at zero
+    if (L->s.gu_acc) {
+      const ds4moe_config& c = L->cfg;
+      const int Tdec = (c.force_path != DS4MOE_PATH_AUTO || c.max_tokens < c.decode_max_tokens) ? c.max_tokens
+                                                                                              : c.decode_max_tokens;
+      if (cudaMemset(L->s.gu_acc, 0, (size_t)Tdec * c.top_k * 2 * c.d_ff * 4) != cudaSuccess ||
+          cudaMemset(L->s.tile_cnt, 0, (size_t)c.n_experts * (c.d_ff / 64) * L->s.dec_maxch * 4) != cudaSuccess ||
+          cudaDeviceSynchronize() != cudaSuccess)
+        return DS4MOE_ERR_CUDA;
+    }
     return DS4MOE_ERR_DEVICE_TIMEOUT;
   }
   return DS4MOE_OK;

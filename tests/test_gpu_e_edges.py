@@ -74,7 +74,7 @@ def test_path_choice_and_launch_counts(ds4, tiny):
     assert layer.launches_per_forward(4) == 3
     assert layer.launches_per_forward(16) == 5
     names = [ds4.lib().ds4moe_kernel_name(layer._h, 4, i) for i in range(4)]
-    assert names == [b"route_small", b"gemm_gateup", b"gemm_down", None]
+    assert names == [b"route_small", b"decode_mma_gateup", b"decode_mma_down", None]
     names = [ds4.lib().ds4moe_kernel_name(layer._h, 16, i) for i in range(6)]
     assert names == [b"route_topk", b"route_group", b"act_quant", b"gemm_gateup", b"gemm_down", None]
 

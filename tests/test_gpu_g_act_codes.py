@@ -81,27 +81,33 @@ def test_x_codes_bit_exact_and_output_on_edge_inputs(ds4, wl, path):
     idx, w = oracle.route(logits.numpy(), wl.k)
     act = oracle.ACT_MXFP8 if path == "prefill" else oracle.ACT_EXACT
     ref = oracle.forward(dims_of(wl), host_weights(W), bf16_bits(x), idx, w, list(range(wl.T)), act)
-    assert_parity(out.cpu().numpy(), ref, f"{wl.name} {path}")
+    out = out.cpu().numpy()
+    # Token 3's dominant element makes its output ~1000x the others', so the
+    # batch rms of the tolerance would be that one token's: it is held to the
+    # tolerance on its own, the other tokens as a batch.
+    rest = [t for t in range(wl.T) if t != 3]
+    assert_parity(out[rest], ref[rest], f"{wl.name} {path} (all tokens but the dominant one)")
+    assert_parity(out[3:4], ref[3:4], f"{wl.name} {path} (dominant token)")
     assert not out[0].any()  # a zero token has a zero output
     layer.close()
 
 
+def _decode_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    return np.array([oracle.e4m3_decode(int(c)) for c in codes]) * np.repeat([oracle.e8m0(int(b)) for b in scales], 32)
+
+
 def _oracle_h(dims, Wh, x_bits, idx, t, j, mode):
     """The oracle's pieces for one routed pair: h = SwiGLU(Wg x^, Wu x^) with
-    x^ = MXFP8(x) (prefill) or x (decode), h rounded to fp32 (the precision the
-    kernel quantises in)."""
+    x^ = MXFP8(x) (prefill) or hi + lo = MXFP8(x) + MXFP8(x - MXFP8(x))
+    (DECODE_MMA: the rows the GPU multiplies, checked byte for byte above), h
+    rounded to fp32 (the precision the kernel quantises in)."""
     e = int(idx[t, j])
     wg, wu, _ = oracle.dequant_expert(dims, Wh, e)
     xv = np.array([oracle.bf16(int(b)) for b in x_bits[t]])
-    if mode == "prefill":
-        c, s = oracle.mxfp8(xv)
-        xv = np.array([oracle.e4m3_decode(int(v)) for v in c]) * np.repeat([oracle.e8m0(int(b)) for b in s], 32)
+    hi = _decode_rows(*oracle.mxfp8(xv))
+    xv = hi if mode == "prefill" else hi + _decode_rows(*oracle.mxfp8(xv - hi))
     g, u = wg @ xv, wu @ xv
     return (g / (1.0 + np.exp(-g)) * u).astype(np.float32).astype(np.float64)
-
-
-def _decode_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    return np.array([oracle.e4m3_decode(int(c)) for c in codes]) * np.repeat([oracle.e8m0(int(b)) for b in scales], 32)
 
 
 @pytest.mark.parametrize("path", ["prefill", "decode_mma"])
