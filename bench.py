@@ -385,21 +385,30 @@ def run_ours(args):
     # ---- the other workloads, same GPU (rank 0 reports them)
     also = {}
     if not args.no_extra:
-        for name in ("decode1", "decode64", "prefill", "q2k"):
+        q2k_layer = None
+        for name in ("decode1", "decode64", "prefill", "q2k", "q2k_decode1", "q2k_decode64"):
             if name == wl.name:
                 continue
             other = synth.WORKLOADS[name]
             try:
-                if other.down == "q2k" or layer_wl.down == "q2k":
-                    Wq = synth.make_layer_weights(other, device="cuda")
-                    lay2 = ds4.Layer(other.d, other.E, other.f, other.k, max(4096, other.T), Wq)
-                    del Wq
+                if other.down == "q2k" and layer_wl.down != "q2k":
+                    if q2k_layer is None:  # one Q2_K layer (weight seed 4) serves its three workloads
+                        qwl = synth.WORKLOADS["q2k"]
+                        Wq = synth.make_layer_weights(qwl, device="cuda")
+                        q2k_layer = ds4.Layer(qwl.d, qwl.E, qwl.f, qwl.k, qwl.T, Wq)
+                        del Wq
+                        torch.cuda.empty_cache()
+                    lay2 = q2k_layer
+                elif other.down != "q2k" and layer_wl.down == "q2k":
+                    Wm = synth.make_layer_weights(other, device="cuda")
+                    lay2 = ds4.Layer(other.d, other.E, other.f, other.k, max(4096, other.T), Wm)
+                    del Wm
                     torch.cuda.empty_cache()
                 else:
                     lay2 = layer
                 fl = L2Flush() if other.T <= 64 else None
                 r, a, *_ = measure_workload(ds4, lay2, other, min(args.steps, 50), args.warmup, peaks, fl)
-                if lay2 is not layer:
+                if lay2 is not layer and lay2 is not q2k_layer:
                     lay2.close()
                     torch.cuda.empty_cache()
                 also[name] = {k: v for k, v in r.items()}
@@ -408,6 +417,9 @@ def run_ours(args):
                     also[name]["l2"] = "flushed (512 MB write + read back) before every step"
             except Exception as exc:  # report, do not hide
                 also[name] = {"error": str(exc)}
+        if q2k_layer is not None:
+            q2k_layer.close()
+            torch.cuda.empty_cache()
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0)
     cpu = None

@@ -95,8 +95,10 @@ enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2, DS
  *   top_k      experts per token k; 1..min(8, E).
  *   max_tokens largest T a forward call may pass (scratch is sized for it).
  *   down_format      DS4MOE_DOWN_MXFP4 or DS4MOE_DOWN_Q2K.  A Q2_K layer runs
- *                    every call on the PREFILL path (the decode paths stream
- *                    MXFP4 only; forcing one of them is then UNSUPPORTED).
+ *                    DECODE_MMA and PREFILL like an MXFP4 one (its down
+ *                    projection multiplies fp16 h by weights dequantised to
+ *                    fp16 on either path); forcing the CUDA-core DECODE path,
+ *                    which streams MXFP4 only, is UNSUPPORTED.
  *   decode_max_tokens  AUTO path choice: T <= this runs DECODE_MMA (default 64).
  *   force_path       DS4MOE_PATH_* (AUTO by default; tests force a path).
  *   debug_fault      0 in production.  1 = in the gate/up GEMM, the first
@@ -209,8 +211,9 @@ int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
  * error.  ds4moe_kernel_name(layer, T, i) names the i-th kernel a forward of
  * T tokens enqueues (NULL past the end):
  *   DECODE:                route_topk, route_group, decode_gateup, decode_down
- *   DECODE_MMA, T <= 4:    route_small, decode_mma_gateup, decode_mma_down
+ *   DECODE_MMA, T <= 4:    route_small, decode_mma_gateup, decode_mma_down (gemm_down for Q2_K)
  *   DECODE_MMA, T > 4:     route_topk, route_group, act_quant, decode_mma_gateup, decode_mma_down
+ *                          (gemm_down for Q2_K)
  *   PREFILL, T <= 4:       route_small, gemm_gateup, gemm_down
  *   PREFILL, T > 4:        route_topk, route_group, act_quant, gemm_gateup, gemm_down */
 int ds4moe_set_kernel_timing(ds4moe_layer *layer, int enable);

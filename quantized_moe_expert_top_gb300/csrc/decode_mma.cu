@@ -85,6 +85,7 @@ struct DArgs {
   int maxch;         // token chunks per expert the counters are sized for
   uint8_t* hq;       // gate/up: MXFP8 h rows (hi, lo) in padded expert order
   uint8_t* hsf;
+  __half* h16;       // gate/up with a Q2_K down projection: fp16 h, row pad_offsets[e] / 2 + token (else null)
   float* out;        // down: [T][d]
   DeviceStatus* status;
   uint64_t budget_ns;
@@ -460,7 +461,14 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
             for (int jj = 0; jj < 8; ++jj) xg[jj * 64 + fq * 32 + lane] = silu_f(val[jj]);
           }
           named_bar_sync(2, 32 * kDEpiWarps);  // silu(g) of the slice staged
-          if (!gate) {
+          if (!gate && args.h16 != nullptr) {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int t = c0 / 2 + jj;
+              if (t < ntok)
+                args.h16[(size_t)(prow0 / 2 + t) * args.f + i] = __float2half_rn(xg[jj * 64 + fq * 32 + lane] * val[jj]);
+            }
+          } else if (!gate) {
             float h[8];
             uint32_t am[8];
 #pragma unroll
@@ -553,6 +561,10 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
               __stcg(src, 0.f);
               __stcg(src + 64, 0.f);
               const float h = silu_f(g[b]) * u[b];
+              if (args.h16 != nullptr) {
+                args.h16[(size_t)(prow0 / 2 + t) * args.f + i] = __float2half_rn(h);
+                continue;
+              }
               // hi = MXFP8(h), lo = MXFP8(h - hi) over the warp's 32 features
               const int sh = mxfp8_exponent(warp_max(fabsf(h)));
               const uint32_t chi = f32x2_to_e4m3x2(h * exp2i(-sh), 0.f) & 0xFFu;
@@ -634,6 +646,7 @@ cudaError_t launch_decmma_gateup(const ds4moe_layer* L, int T, cudaStream_t st) 
   a.maxch = L->s.dec_maxch;
   a.hq = L->s.hq;
   a.hsf = L->s.hsf;
+  a.h16 = L->cfg.down_format == DS4MOE_DOWN_Q2K ? L->s.h16 : nullptr;
   return launch_dec<DMode::GateUp>(L, m, a, T, st);
 }
 

@@ -82,7 +82,8 @@ struct Scratch {
   uint8_t* xsf;          // [d/128][pad_rows_max/128][512] E8M0 scales (tcgen05 chunk layout)
   uint8_t* hq;           // [pad_rows_max][f]   MXFP8 codes of h (MXFP4 down)
   uint8_t* hsf;          // [f/128][pad_rows_max/128][512]
-  __half* h16;           // [pad_rows_max][f]   fp16 h (Q2_K down)
+  __half* h16;           // [pad_rows_max][f]   fp16 h (Q2_K down); one row per routed pair, expert e's
+                         //   first at pad_offsets[e] / (padded rows per pair)
   float* gu_acc;         // [Tdec*k][2f] DECODE_MMA gate/up partial sums (zero between calls)
   int32_t* tile_cnt;     // [E][f/64][dec_maxch] K slices done per gate/up tile and token chunk
   int dec_maxch;         // 128-row token chunks per expert at the DECODE_MMA token limit
@@ -171,7 +172,9 @@ cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStr
 cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStream_t st);
 cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st);
-cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+// rpp = padded activation rows per routed pair of the routing that preceded
+// (1 on the PREFILL path, 2 on DECODE_MMA); h16 holds one row per pair.
+cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, int rpp, cudaStream_t st);
 // DECODE_MMA grouped GEMMs (one CTA per SM, split-K over the touched experts'
 // weight tiles); the activation rows are split (hi, lo) as above.
 cudaError_t launch_decmma_gateup(const ds4moe_layer* L, int T, cudaStream_t st);

@@ -208,7 +208,6 @@ int alloc(ds4moe_layer* L, Tp** p, size_t bytes) {
 }
 
 int path_of(const ds4moe_layer* L, int T) {
-  if (L->cfg.down_format == DS4MOE_DOWN_Q2K) return DS4MOE_PATH_PREFILL;  // decode paths stream MXFP4 only
   if (L->cfg.force_path != DS4MOE_PATH_AUTO) return L->cfg.force_path;
   return T <= L->cfg.decode_max_tokens ? DS4MOE_PATH_DECODE_MMA : DS4MOE_PATH_PREFILL;
 }
@@ -226,8 +225,9 @@ int kernel_list(const ds4moe_layer* L, int T, const char** names) {
       for (const char* k : {"route_topk", "route_group", "act_quant"}) names[n++] = k;
     }
     const bool dm = path == DS4MOE_PATH_DECODE_MMA;
+    const bool q2k = L->cfg.down_format == DS4MOE_DOWN_Q2K;
     names[n++] = dm ? "decode_mma_gateup" : "gemm_gateup";
-    names[n++] = dm ? "decode_mma_down" : "gemm_down";
+    names[n++] = (dm && !q2k) ? "decode_mma_down" : "gemm_down";
   }
   return n;
 }
@@ -292,15 +292,15 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   const size_t dn_codes = (size_t)E * d * (f / 2), dn_scales = (size_t)E * d * (f / 32);
   const int64_t pairs = (int64_t)Tm * k;
   const bool q2k = cfg->down_format == DS4MOE_DOWN_Q2K;
-  if (q2k && (cfg->force_path == DS4MOE_PATH_DECODE || cfg->force_path == DS4MOE_PATH_DECODE_MMA)) {
-    delete L;  // the decode paths stream MXFP4 only
+  if (q2k && cfg->force_path == DS4MOE_PATH_DECODE) {
+    delete L;  // the CUDA-core GEMV streams MXFP4 only
     return DS4MOE_ERR_UNSUPPORTED;
   }
   // GEMV buffers only when that path is forced; the GEMM buffers serve PREFILL and DECODE_MMA.
   const bool need_dec = !q2k && cfg->force_path == DS4MOE_PATH_DECODE;
   const bool need_pre = cfg->force_path != DS4MOE_PATH_DECODE;
-  const bool split_ok = !q2k && (cfg->force_path == DS4MOE_PATH_DECODE_MMA ||
-                                 (cfg->force_path == DS4MOE_PATH_AUTO && cfg->decode_max_tokens > 0));
+  const bool split_ok = cfg->force_path == DS4MOE_PATH_DECODE_MMA ||
+                        (cfg->force_path == DS4MOE_PATH_AUTO && cfg->decode_max_tokens > 0);
   const int Tdec = (cfg->force_path != DS4MOE_PATH_AUTO || Tm < cfg->decode_max_tokens) ? Tm
                                                                                        : cfg->decode_max_tokens;
   // padded activation rows: one per routed pair (PREFILL), two (DECODE_MMA)
@@ -427,20 +427,22 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
         tm_ok = tm_ok && encode_sf_weights(&L->tm_sfa_dn, w.down_sf, (uint64_t)E * (d / 128) * (f / 128));
         tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h, s.hsf, r128, (uint64_t)f / 128);
       }
-      if (split_ok && !q2k) {
+      if (split_ok) {
+        // gate/up side (both down formats), then the MXFP4 down side
         tm_ok = tm_ok && encode_3d_kblocks(&L->tm_gu3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu,
                                            (uint64_t)E * f * 2, (uint64_t)d / 128, w.pitch_gu, 64, 128);
-        tm_ok = tm_ok && encode_3d_kblocks(&L->tm_dn3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn,
-                                           (uint64_t)E * d, (uint64_t)f / 128, w.pitch_dn, 64, 128);
-        for (int b = 0; b < 8; ++b) {
-          const uint32_t rows = 16u * (uint32_t)(b + 1);
+        for (int b = 0; b < 8; ++b)
           tm_ok = tm_ok && encode_3d_kblocks(&L->tm_xq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, pad_rows,
-                                             (uint64_t)d / 128, d, 128, rows);
-          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_hq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, pad_rows,
-                                             (uint64_t)f / 128, f, 128, rows);
-        }
+                                             (uint64_t)d / 128, d, 128, 16u * (uint32_t)(b + 1));
         tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_x1, s.xsf, r128, (uint64_t)d / 128, 1);
-        tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h1, s.hsf, r128, (uint64_t)f / 128, 1);
+        if (!q2k) {
+          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_dn3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn,
+                                             (uint64_t)E * d, (uint64_t)f / 128, w.pitch_dn, 64, 128);
+          for (int b = 0; b < 8; ++b)
+            tm_ok = tm_ok && encode_3d_kblocks(&L->tm_hq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, pad_rows,
+                                               (uint64_t)f / 128, f, 128, 16u * (uint32_t)(b + 1));
+          tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h1, s.hsf, r128, (uint64_t)f / 128, 1);
+        }
         L->decmma_ready = tm_ok;
       }
       if (!tm_ok) {
@@ -528,15 +530,14 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
       if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
       if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, split, st));
     }
+    const bool q2k = L->cfg.down_format == DS4MOE_DOWN_Q2K;
     if (path == DS4MOE_PATH_DECODE_MMA) {
       if (e == cudaSuccess) e = mark(launch_decmma_gateup(L, T, st));
-      if (e == cudaSuccess) e = mark(launch_decmma_down(L, out, T, st));
+      if (e == cudaSuccess) e = mark(q2k ? launch_gemm_down_q2k(L, out, T, 2, st) : launch_decmma_down(L, out, T, st));
     } else {
       if (e == cudaSuccess) e = mark(launch_gemm_gateup(L, T, split, st));
-      if (e == cudaSuccess) {
-        if (L->cfg.down_format == DS4MOE_DOWN_Q2K) e = mark(launch_gemm_down_q2k(L, out, T, st));
-        else e = mark(launch_gemm_down(L, out, T, split, st));
-      }
+      if (e == cudaSuccess)
+        e = mark(q2k ? launch_gemm_down_q2k(L, out, T, 1, st) : launch_gemm_down(L, out, T, split, st));
     }
   }
   L->last_nk = nk - 1;

@@ -125,6 +125,8 @@ struct Q2kArgs {
   const int32_t* pad_pair;
   const float* topk_w;
   int E, k, d, f;
+  int rpp;       // padded activation rows per routed pair (1, or 2 on the few-token path); h has one
+                 // row per pair, expert e's first at pad_offsets[e] / rpp
   float* out;
   DeviceStatus* status;
   uint64_t budget_ns;
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
       for (bool more = it.first_chunk(); more && ok; more = it.next()) {
         const int N = round16(it.nch);
         const CUtensorMap* tb = &bmaps.m[N / 16 - 1];  // one box of exactly N token rows
-        const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+        const int prow = __ldg(args.pad_offsets + it.e) / args.rpp + it.t0;  // h row of the chunk's first token
         const uint32_t bytes = (uint32_t)N * 128u;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
     int chunk = 0;
     for (bool more = it.first_chunk(); more; more = it.next(), ++chunk) {
       const int N = round16(it.nch);
-      const int prow = __ldg(args.pad_offsets + it.e) + it.t0;
+      const int prow = __ldg(args.pad_offsets + it.e) + it.t0 * args.rpp;  // padded row of the chunk's first token
       const int buf = chunk & 1;
       // Per-column token and routing weight, loaded while the MMAs run.  One
       // thread takes the accumulator wait and publishes the outcome, so all
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
       // one of them).
       named_bar_sync(1, 32 * kQEpiWarps);  // previous chunk's table no longer read
       for (int c = etid; c < it.nch; c += 32 * kQEpiWarps) {
-        const int pr = __ldg(args.pad_pair + prow + c);
+        const int pr = __ldg(args.pad_pair + prow + c * args.rpp);
         col_tok[c] = pr / args.k;
         col_w[c] = __ldg(args.topk_w + pr);
       }
@@ -521,7 +523,7 @@ cudaError_t launch_act_quant(const ds4moe_layer* L, const void* x, float* out, i
                     L->cfg.top_k, L->s.pad_inv, L->s.xq, L->s.xsf, (int)(L->s.pad_rows_max / 128), split, out);
 }
 
-cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaStream_t st) {
+cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, int rpp, cudaStream_t st) {
   (void)T;
   static InitOnce attr_once;
   cudaError_t e = init_once(attr_once, [] {
@@ -542,6 +544,7 @@ cudaError_t launch_gemm_down_q2k(const ds4moe_layer* L, float* out, int T, cudaS
   a.k = L->cfg.top_k;
   a.d = L->cfg.d_model;
   a.f = L->cfg.d_ff;
+  a.rpp = rpp;
   a.out = out;
   a.status = L->status;
   a.budget_ns = (uint64_t)L->cfg.wait_timeout_ms * 1000000ull;

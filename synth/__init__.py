@@ -17,6 +17,7 @@ decode1    1     4096   256  2048  8  N(0,1), tie-free jitter
 decode64   64    4096   256  2048  8  N(0,1) + log Zipf(1.1) prior (global)
 prefill    4096  4096   256  2048  8  N(0,1), uniform routing
 q2k        2048  4096   256  2048  8  N(0,1); down projection in Q2_K
+q2k_dec..  1/64  4096   256  2048  8  the q2k layer with the decode1 / decode64 recipes
 =========  ====  =====  ===  ====  =  ==========================================
 
 The 4096-token prefill chunk is the distributed-prefill chunk of
@@ -88,6 +89,9 @@ WORKLOADS = {
     # expert still receives about 128 tokens (the per-expert GEMM shape of the
     # 4096-token chunk) while the device holds well under 1 GB
     "prefill_e32": Workload("prefill_e32", 512, 4096, 32, 2048, 8, 3, 1, "normal"),
+    # the Q2_K layer (weight seed 4) at one token and at 64 tokens with a Zipf prior
+    "q2k_decode1": Workload("q2k_decode1", 1, 4096, 256, 2048, 8, 1, 4, "normal", "q2k"),
+    "q2k_decode64": Workload("q2k_decode64", 64, 4096, 256, 2048, 8, 2, 4, "zipf", "q2k"),
     # profiling cases of the few-token and Q2_K paths with fewer experts (the
     # per-expert shapes of the full workloads, a fraction of the device memory)
     "decode1_e32": Workload("decode1_e32", 1, 4096, 32, 2048, 8, 1, 1, "normal"),
