@@ -79,8 +79,11 @@ __global__ void pack_rows_kernel(uint8_t* __restrict__ dst, int pitch, int64_t r
 
 // Q2_K super-blocks [E][d][f/256][84] -> tile-major chunks [E][d/128][f/64]
 // of 3072 bytes: for row r of the 128-row block and K step kb (64 weights,
-// quarter kb % 4 of super-block kb / 4): bytes 16r.. the 16 code bytes of that
-// quarter, 2048 + 4r.. its 4 sub-block scale bytes, 2560 + 4r.. d | dmin.
+// quarter kb % 4 of super-block kb / 4): bytes 16r.. four 32-bit words, one
+// per 16-weight sub-block, holding the 2-bit code of local weight i at bit
+// 2i for even i and 16 + 2(i - 1) for odd i (so one shift and mask yields the
+// codes of two neighbouring weights in the two 16-bit halves); 2048 + 4r..
+// the 4 sub-block scale bytes; 2560 + 4r.. d | dmin.
 __global__ void repack_q2k_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int d, int f) {
   const int KB = f / 64, nsb = f / 256;
   const size_t total = (size_t)E * d * KB;  // one thread per (expert, row, K step)
@@ -92,7 +95,15 @@ __global__ void repack_q2k_kernel(const uint8_t* __restrict__ src, uint8_t* __re
     const uint8_t* blk = src + (((size_t)e * d + row) * nsb + kb / 4) * 84;
     const int q4 = kb % 4, r = row % 128;
     uint8_t* ch = dst + (((size_t)e * (d / 128) + row / 128) * KB + kb) * kQ2kChunk;
-    for (int b = 0; b < 16; ++b) ch[16 * r + b] = blk[16 + 16 * q4 + b];
+    for (int sb = 0; sb < 4; ++sb) {
+      uint32_t word = 0;
+      for (int i = 0; i < 16; ++i) {  // weight 64 q4 + 16 sb + i of the super-block
+        const int wi = 64 * q4 + 16 * sb + i;
+        const uint32_t qc = (blk[16 + wi / 4] >> (2 * (wi % 4))) & 3u;
+        word |= qc << ((i & 1) * 16 + 2 * (i >> 1));
+      }
+      for (int b = 0; b < 4; ++b) ch[16 * r + 4 * sb + b] = (uint8_t)(word >> (8 * b));
+    }
     for (int b = 0; b < 4; ++b) ch[2048 + 4 * r + b] = blk[4 * q4 + b];
     for (int b = 0; b < 4; ++b) ch[2560 + 4 * r + b] = blk[80 + b];
   }

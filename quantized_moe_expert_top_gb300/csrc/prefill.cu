@@ -13,8 +13,9 @@
 //
 // The Q2_K GEMM is persistent, one CTA per SM: warp 0 issues the TMA loads of
 // h, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 drain the
-// double-buffered accumulator, warps 10..13 dequantise, the last warp copies
-// the Q2_K chunks with cp.async.  Every mbarrier wait is bounded; a wait that
+// double-buffered accumulator, warps 10..17 dequantise (two threads per weight
+// row), the last warp streams the Q2_K chunks with bulk copies into a ring of
+// kQRaw slots that runs far ahead of the dequantisation.  Every mbarrier wait is bounded; a wait that
 // runs out records DS4MOE_ERR_DEVICE_TIMEOUT in the layer's status word and
 // the CTA drains its in-flight copies and MMAs (again bounded) before it exits.
 #include "gemm.cuh"
@@ -96,10 +97,11 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
 // --------------------------------------------------------------- Q2_K down GEMM
 // Tensor memory (512 columns): accumulator buffers at columns 0 and 256.  One
 // pipeline stage covers 64 contraction elements (128 bytes of fp16 per row).
-constexpr int kQNMax = 192;      // token columns per chunk
+constexpr int kQNMax = 128;      // token columns per chunk
 constexpr int kQStages = 4;
+constexpr int kQRaw = 28;        // slots of the raw Q2_K chunk ring (84 KB of weights in flight)
 constexpr int kQKs = 64;         // fp16 elements per stage
-constexpr int kQDeqWarps = 4;    // one weight row per thread
+constexpr int kQDeqWarps = 8;    // two threads per weight row, two 16-weight sub-blocks each
 constexpr int kQEpiWarps = 8;    // two per tensor-memory lane quarter
 constexpr int kQAcc1 = 256;
 constexpr int kQThreads = 64 + 32 * kQEpiWarps + 32 * kQDeqWarps + 32;
@@ -108,14 +110,15 @@ static_assert(kQAcc1 + kQNMax <= 512, "tensor memory");
 struct QSmem {
   static constexpr int kA = kBM * 128;       // fp16 weight tile, 128-byte swizzled rows
   static constexpr int kB = kQNMax * 128;    // fp16 token tile
-  static constexpr int kChunk = 4096;        // Q2_K chunk (3072 bytes) + pad
-  static constexpr int kStage = kA + kB + kChunk;
-  static constexpr int kColOff = kQStages * kStage;  // per-column (token, routing weight)
+  static constexpr int kStage = kA + kB;
+  static constexpr int kRawOff = kQStages * kStage;  // raw Q2_K chunks, kQ2kChunk bytes each
+  static constexpr int kColOff = kRawOff + kQRaw * kQ2kChunk;  // per-column (token, routing weight)
   static constexpr int kBarOff = kColOff + kQNMax * 8;
-  static constexpr int kTotal = kBarOff + 256 + 1024;
+  static constexpr int kTotal = kBarOff + 1024 + 1024;  // barriers (17 + 2 * kQRaw) and flags, alignment slack
 };
 static_assert(QSmem::kStage % 1024 == 0, "stage alignment");
 static_assert(QSmem::kTotal <= 227 * 1024, "shared memory");
+static_assert((17 + 2 * kQRaw) * 8 + 16 <= 1024, "barrier area");
 
 struct Q2kArgs {
   const uint8_t* q2k;  // tile-major chunks [E][d/128][f/64][3072]
@@ -165,24 +168,6 @@ struct QIter {
   }
 };
 
-// The same sequence one pipeline stage at a time (the helper's L2 prefetch
-// cursor runs kQPrefetch stages ahead of its copies).
-struct QStage {
-  QIter it;
-  int kb, KB;
-  bool valid;
-  __device__ void start() {
-    kb = 0;
-    valid = it.first_chunk();
-  }
-  __device__ void next() {
-    if (!valid) return;
-    if (++kb < KB) return;
-    kb = 0;
-    valid = it.next();
-  }
-};
-constexpr int kQPrefetch = 8;  // Q2_K chunks prefetched into L2 ahead of their copy
 
 __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_constant__ BoxMaps bmaps,
                                                               const Q2kArgs args) {
@@ -197,9 +182,12 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
   uint64_t* acc_full = afull + kQStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;     // [2]
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* raw_full = drain + 1;         // [kQRaw] raw chunk landed
+  uint64_t* raw_empty = raw_full + kQRaw;  // [kQRaw] raw chunk dequantised
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + kQRaw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_ok = abort_flag + 1;
+  uint8_t* raw = smem + S::kRawOff;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mb_per_e = args.d / kBM;
@@ -207,9 +195,13 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&full[s], 1 + 32);  // producer (TMA bytes) + helper lanes (cp.async)
+      mbar_init(&full[s], 1);  // producer (TMA bytes of h)
       mbar_init(&empty[s], 1);
       mbar_init(&afull[s], kQDeqWarps);
+    }
+    for (int s = 0; s < kQRaw; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kQDeqWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -327,56 +319,60 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
     }
     __syncwarp();
   } else if (warp == kHelperWarp) {
-    // ------------------------------------------------------------ Q2_K chunks by cp.async
-    QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
-    QStage pf{it, 0, KB, false};
-    pf.start();
-    auto l2_prefetch = [&]() {
-      if (pf.valid && lane < kQ2kChunk / 128)
-        prefetch_l2(args.q2k + ((size_t)(pf.it.e * mb_per_e + pf.it.mb) * KB + pf.kb) * kQ2kChunk + lane * 128);
-      pf.next();
-    };
-    for (int i = 0; i < kQPrefetch; ++i) l2_prefetch();
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (bool more = it.first_chunk(); more && ok; more = it.next()) {
-      for (int kb = 0; kb < KB; ++kb) {
-        uint32_t got = 0;
-        if (lane == 0) got = mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag) ? 1u : 0u;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          if (lane == 0) {
+    // ------------------------------------------------------------ raw Q2_K chunks, one bulk copy each
+    // The ring runs up to kQRaw steps ahead of the dequantisation, so that many
+    // kilobytes of weights are in flight per SM.
+    if (lane == 0) {
+      QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
+      int slot = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
+        const uint8_t* src = args.q2k + (size_t)(it.e * mb_per_e + it.mb) * KB * kQ2kChunk;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&raw_empty[slot], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
             *abort_flag = 1;
+            ok = false;
+            break;
           }
-          ok = false;
-          break;
-        }
-        uint8_t* dst = smem + stage * S::kStage + S::kA + S::kB;
-        const uint8_t* src = args.q2k + ((size_t)(it.e * mb_per_e + it.mb) * KB + kb) * kQ2kChunk;
-        for (int i = lane; i < kQ2kChunk / 16; i += 32) cp_async_16(dst + 16 * i, src + 16 * i);
-        cp_async_arrive_noinc(&full[stage]);
-        l2_prefetch();
-        if (++stage == kQStages) {
-          stage = 0;
-          phase ^= 1u;
+          mbar_arrive_expect_tx(&raw_full[slot], kQ2kChunk);
+          bulk_load(raw + slot * kQ2kChunk, src + (size_t)kb * kQ2kChunk, kQ2kChunk, &raw_full[slot]);
+          ++issued;
+          if (++slot == kQRaw) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       }
+      // every issued copy lands before the CTA exits: the last one of each slot
+      for (uint32_t n = 0; n < kQRaw && n < issued; ++n) {
+        const uint32_t seq = issued - 1 - n;  // a copy still possibly in flight
+        volatile int no_abort = 0;
+        mbar_wait_bounded(&raw_full[seq % kQRaw], (seq / kQRaw) & 1u, args.budget_ns, &no_abort);
+      }
     }
-    cp_async_wait_all();  // this warp's copies land before the CTA may exit
+    __syncwarp();
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ Q2_K -> fp16 weight tile
-    const int r = (warp - kDeqWarp0) * 32 + lane;  // weight row of the 128-row tile
+    const int dt = (warp - kDeqWarp0) * 32 + lane;
+    const int r = dt & 127;   // weight row of the 128-row tile
+    const int half = dt >> 7;  // sub-blocks 2 half, 2 half + 1 of each 64-weight step
     QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     const __half2 k1024 = __float2half2_rn(1024.f);
+    int rslot = 0;
+    uint32_t rphase = 0;
     for (bool more = it.first_chunk(); more && ok; more = it.next()) {
       for (int kb = 0; kb < KB; ++kb) {
         uint32_t got = 0;
-        if (lane == 0) got = mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag) ? 1u : 0u;
+        if (lane == 0)
+          got = (mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag) &&
+                 mbar_wait_bounded(&raw_full[rslot], rphase, args.budget_ns, abort_flag))
+                    ? 1u
+                    : 0u;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           if (lane == 0) {
@@ -387,38 +383,42 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
           break;
         }
         uint8_t* st = smem + stage * S::kStage;
-        const uint8_t* ch = st + S::kA + S::kB;
-        const uint4 qv = *reinterpret_cast<const uint4*>(ch + 16 * r);
-        const uint32_t scw = *reinterpret_cast<const uint32_t*>(ch + 2048 + 4 * r);
+        const uint8_t* ch = raw + rslot * kQ2kChunk;
+        const uint2 qv = *reinterpret_cast<const uint2*>(ch + 16 * r + 8 * half);
+        const uint32_t scw = *reinterpret_cast<const uint16_t*>(ch + 2048 + 4 * r + 2 * half);
         const uint32_t ddw = *reinterpret_cast<const uint32_t*>(ch + 2560 + 4 * r);
         const float dd = __half2float(__ushort_as_half((unsigned short)(ddw & 0xFFFFu)));
         const float dm = __half2float(__ushort_as_half((unsigned short)(ddw >> 16)));
-        const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+        const uint32_t words[2] = {qv.x, qv.y};
         uint8_t* arow = st + r * 128;
 #pragma unroll
-        for (int sb = 0; sb < 4; ++sb) {  // sub-block sb = weights 16 sb .. 16 sb + 15 of the step
-          const uint32_t scb = (scw >> (8 * sb)) & 0xFFu;
+        for (int j = 0; j < 2; ++j) {  // sub-block sb = 2 half + j: weights 16 sb .. 16 sb + 15 of the step
+          const int sb = 2 * half + j;
+          const uint32_t scb = (scw >> (8 * j)) & 0xFFu;
           const __half2 a2 = __float2half2_rn(dd * (float)(scb & 15u));
           const __half2 nb2 = __float2half2_rn(-dm * (float)(scb >> 4));
-          uint32_t P[8];  // P[n] = {w_n, w_(n+8)}: 2-bit codes 16 bits apart in the word
+          uint32_t P[8];  // P[n] = {w_2n, w_2n+1}: the repacked word holds w_2n at bit 2n, w_2n+1 at bit 16 + 2n
 #pragma unroll
           for (int n = 0; n < 8; ++n) {
-            const uint32_t v = ((words[sb] >> (2 * n)) & 0x00030003u) | 0x64006400u;  // f16 1024 + q
+            const uint32_t v = ((words[j] >> (2 * n)) & 0x00030003u) | 0x64006400u;  // f16 1024 + q
             const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&v), k1024);
             const __half2 w2 = __hfma2(q2, a2, nb2);
             P[n] = *reinterpret_cast<const uint32_t*>(&w2);
           }
-          const uint4 lo = make_uint4(__byte_perm(P[0], P[1], 0x5410), __byte_perm(P[2], P[3], 0x5410),
-                                      __byte_perm(P[4], P[5], 0x5410), __byte_perm(P[6], P[7], 0x5410));
-          const uint4 hi = make_uint4(__byte_perm(P[0], P[1], 0x7632), __byte_perm(P[2], P[3], 0x7632),
-                                      __byte_perm(P[4], P[5], 0x7632), __byte_perm(P[6], P[7], 0x7632));
           // 16-byte chunks 2 sb and 2 sb + 1 of the row, 128-byte swizzle
-          *reinterpret_cast<uint4*>(arow + (((2 * sb) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(arow + (((2 * sb + 1) ^ (r & 7)) << 4)) = hi;
+          *reinterpret_cast<uint4*>(arow + (((2 * sb) ^ (r & 7)) << 4)) = make_uint4(P[0], P[1], P[2], P[3]);
+          *reinterpret_cast<uint4*>(arow + (((2 * sb + 1) ^ (r & 7)) << 4)) = make_uint4(P[4], P[5], P[6], P[7]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[stage]);
+        if (lane == 0) {
+          mbar_arrive(&afull[stage]);
+          mbar_arrive(&raw_empty[rslot]);  // this warp's reads of the raw chunk are done
+        }
+        if (++rslot == kQRaw) {
+          rslot = 0;
+          rphase ^= 1u;
+        }
         if (++stage == kQStages) {
           stage = 0;
           phase ^= 1u;
