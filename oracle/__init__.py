@@ -74,6 +74,10 @@ def lib():
             L.ds4o_dequant_expert.restype = None
             L.ds4o_dequant_expert.argtypes = [i, i, i, i, i] + [u8p] * 7 + [dp, dp, dp]
             L.ds4o_num_threads.restype = i; L.ds4o_num_threads.argtypes = []
+            L.ds4o_router_logits.restype = None
+            L.ds4o_router_logits.argtypes = [i, i, u16p, u16p, i, dp]
+            L.ds4o_shared_ffn.restype = None
+            L.ds4o_shared_ffn.argtypes = [i, i, u16p, u16p, u16p, u16p, i, i32p, dp]
             _lib = L
     return _lib
 
@@ -197,6 +201,32 @@ def dequant_expert(dims, W, e: int):
     lib().ds4o_dequant_expert(d, dims["E"], f, down_fmt, e, *ptrs,
                               _p(wg, ctypes.c_double), _p(wu, ctypes.c_double), _p(wd, ctypes.c_double))
     return wg, wu, wd
+
+
+# ---------------------------------------------------------------- router and shared expert
+def router_logits(wr_bits: np.ndarray, x_bits: np.ndarray) -> np.ndarray:
+    """fp64 router logits [T, E] of bf16 weights wr [E, d] and bf16 x [T, d]."""
+    wr = np.ascontiguousarray(wr_bits, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    E, d = wr.shape
+    T = x.shape[0]
+    out = np.empty((T, E), np.float64)
+    lib().ds4o_router_logits(d, E, _p(wr, ctypes.c_uint16), _p(x, ctypes.c_uint16), T, _p(out, ctypes.c_double))
+    return out
+
+
+def shared_ffn(wg_bits, wu_bits, wd_bits, x_bits, tokens) -> np.ndarray:
+    """Shared-expert output (fp64) for the listed tokens: [len(tokens), d]."""
+    wg = np.ascontiguousarray(wg_bits, dtype=np.uint16)
+    wu = np.ascontiguousarray(wu_bits, dtype=np.uint16)
+    wd = np.ascontiguousarray(wd_bits, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    fs, d = wg.shape
+    tokens = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    y = np.empty((tokens.size, d), np.float64)
+    lib().ds4o_shared_ffn(d, fs, _p(wg, ctypes.c_uint16), _p(wu, ctypes.c_uint16), _p(wd, ctypes.c_uint16),
+                          _p(x, ctypes.c_uint16), tokens.size, _p(tokens, ctypes.c_int32), _p(y, ctypes.c_double))
+    return y
 
 
 def num_threads() -> int:

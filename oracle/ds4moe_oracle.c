@@ -21,6 +21,9 @@
  *             pairs stably sorted by (expert, token).
  *   expert  : g = Wg.x, u = Wu.x, h = silu(g)*u = g/(1+exp(-g))*u, y = Wd.h.
  *   combine : out[t] = sum_j w[t,j] * y[t,j].
+ *   with a router and a shared expert (original precision, bf16 weights):
+ *             logits = Wr.x before the routing, and out[t] += the shared
+ *             expert's SwiGLU FFN of x (its h rounded to bf16).
  *
  * Formats (OCP Microscaling Formats v1.0): E2M1 magnitudes
  * {0,0.5,1,1.5,2,3,4,6} with bit 3 the sign; E8M0 byte b -> 2^(b-127)
@@ -383,6 +386,70 @@ void ds4o_dequant_expert(int d, int E, int f, int down_fmt, int e,
             }
         }
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* router projection and shared expert (original precision, bf16)      */
+/* ------------------------------------------------------------------ */
+/* "DwarfStar実地分析", §GGUFの対応範囲は意図的に狭い: the shared expert, the
+ * projections and the routing stay at original precision; only the routed
+ * experts are quantised.  Weights and activations here are bf16.
+ *
+ * Router: logits[t][e] = sum_c Wr[e][c] * x[t][c], exact in fp64 (the caller
+ * rounds to fp32, the precision the kernel takes the top-k decision in). */
+void ds4o_router_logits(int d, int E, const uint16_t *wr, const uint16_t *x, int T, double *logits)
+{
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += ds4o_bf16(wr[(size_t)e * d + c]) * ds4o_bf16(x[(size_t)t * d + c]);
+            logits[(size_t)t * E + e] = acc;
+        }
+}
+
+/* bf16 round-to-nearest-even of an fp32 value, returned as its value. */
+static double bf16_round(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    uint32_t lsb = (u >> 16) & 1u;
+    u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;
+    float r;
+    memcpy(&r, &u, 4);
+    return (double)r;
+}
+
+/* Shared expert for the listed tokens: y[q][m] = sum_i Wd[m][i] * h_i with
+ * g = Wg.x, u = Wu.x (fp64), h = bf16(fp32(g/(1+exp(-g))*u)) -- h kept in
+ * bf16 like the model's activations, the rounding decided on fp32 h as the
+ * kernel does.  Wg, Wu [fs][d], Wd [d][fs] bf16. */
+void ds4o_shared_ffn(int d, int fs, const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
+                     const uint16_t *x, int n, const int32_t *tokens, double *y)
+{
+    double *xin = (double *)malloc(sizeof(double) * (size_t)d);
+    double *h = (double *)malloc(sizeof(double) * (size_t)fs);
+    for (int q = 0; q < n; ++q) {
+        const int t = tokens[q];
+        for (int c = 0; c < d; ++c) xin[c] = ds4o_bf16(x[(size_t)t * d + c]);
+        #pragma omp parallel for schedule(static)
+        for (int i = 0; i < fs; ++i) {
+            double g = 0.0, u = 0.0;
+            for (int c = 0; c < d; ++c) {
+                g += ds4o_bf16(wg[(size_t)i * d + c]) * xin[c];
+                u += ds4o_bf16(wu[(size_t)i * d + c]) * xin[c];
+            }
+            h[i] = bf16_round((float)(g / (1.0 + exp(-g)) * u));
+        }
+        #pragma omp parallel for schedule(static)
+        for (int m = 0; m < d; ++m) {
+            double acc = 0.0;
+            for (int i = 0; i < fs; ++i) acc += ds4o_bf16(wd[(size_t)m * fs + i]) * h[i];
+            y[(size_t)q * d + m] = acc;
+        }
+    }
+    free(xin);
+    free(h);
 }
 
 /* MXFP8 of n values (n % 32 == 0): codes[n], scales[n/32]. */

@@ -375,3 +375,57 @@ def test_q2k_two_superblocks_forward_closed_form(oracle_lib, mode):
     want = np.zeros(d)
     want[:len(g["row_sums"])] = [h * s for s in g["row_sums"]]
     assert np.allclose(out[0], want, rtol=1e-14, atol=0)
+
+
+# ----------------------------------------------------------------- router projection and shared expert
+def _bf16_bits_np(a: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_router_logits_closed_form(oracle_lib):
+    d = 64
+    wr = np.zeros((3, d), np.float32)
+    wr[0] = 1.0
+    wr[1, ::2], wr[1, 1::2] = 1.0, -1.0
+    wr[2, :32], wr[2, 32:] = 0.5, 2.0
+    x = np.ones((2, d), np.float32)
+    x[1, :32] = -1.0
+    got = oracle_lib.router_logits(_bf16_bits_np(wr), _bf16_bits_np(x))
+    # token 0: 64, 0, 16 + 64 = 80; token 1: -32 + 32 = 0, (-1 + 1)*16 + (1 - 1)*16 = 0, -16 + 64 = 48
+    assert got.tolist() == [[64.0, 0.0, 80.0], [0.0, 0.0, 48.0]]
+
+
+def test_router_logits_against_torch_float64(oracle_lib):
+    g = torch.Generator().manual_seed(11)
+    wr = (torch.randn(16, 256, generator=g) / 16).to(torch.bfloat16)
+    x = torch.randn(5, 256, generator=g).to(torch.bfloat16)
+    got = oracle_lib.router_logits(wr.view(torch.int16).numpy().view(np.uint16), x.view(torch.int16).numpy().view(np.uint16))
+    ref = (x.double() @ wr.double().T).numpy()
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_shared_ffn_closed_form(oracle_lib):
+    # gate 1.0, up 0.5, down 1.0, x = 1: g = 32, u = 16, h = bf16(fp32(silu(32) * 16)) = 512, y = 32 * 512
+    d = fs = 32
+    ones = np.ones((fs, d), np.float32)
+    y = oracle_lib.shared_ffn(_bf16_bits_np(ones), _bf16_bits_np(0.5 * ones), _bf16_bits_np(ones),
+                              _bf16_bits_np(np.ones((1, d), np.float32)), [0])
+    assert y.tolist() == [[16384.0] * d]
+
+
+def test_shared_ffn_against_torch_float64(oracle_lib):
+    """The shared expert against torch: fp64 matmuls, SwiGLU, h rounded to fp32
+    then bf16 by torch's casts (round to nearest even)."""
+    g = torch.Generator().manual_seed(12)
+    d, fs = 128, 96
+    wg = (torch.randn(fs, d, generator=g) * 0.05).to(torch.bfloat16)
+    wu = (torch.randn(fs, d, generator=g) * 0.05).to(torch.bfloat16)
+    wd = (torch.randn(d, fs, generator=g) * 0.05).to(torch.bfloat16)
+    x = torch.randn(3, d, generator=g).to(torch.bfloat16)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    y = oracle_lib.shared_ffn(bits(wg), bits(wu), bits(wd), bits(x), [0, 2])
+    xs = x.double()[[0, 2]]
+    gg, uu = xs @ wg.double().T, xs @ wu.double().T
+    h = (torch.nn.functional.silu(gg) * uu).float().to(torch.bfloat16).double()
+    ref = (h @ wd.double().T).numpy()
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
