@@ -228,6 +228,14 @@ class L2Flush:
         torch.sum(self.buf, dim=0, keepdim=True, out=self.sink)
 
 
+def run_forward(layer, x, logits, out):
+    """One forward: given logits, or (logits None) the whole layer from x."""
+    if logits is None:
+        layer.forward_x(x, out)
+    else:
+        layer.forward(x, logits, out)
+
+
 def time_steps(layer, x, logits, out, steps, flush=None, kernel_times=False):
     """Times `steps` forwards with CUDA events on the current stream; returns
     (per-step ms list, per-kernel ms dict of lists)."""
@@ -240,7 +248,7 @@ def time_steps(layer, x, logits, out, steps, flush=None, kernel_times=False):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        layer.forward(x, logits, out)
+        run_forward(layer, x, logits, out)
         e1.record(st)
         e1.synchronize()
         per_step.append(e0.elapsed_time(e1))
@@ -259,14 +267,14 @@ def routing_counts(wl: synth.Workload, logits: torch.Tensor) -> np.ndarray:
 
 
 # ----------------------------------------------------------------- our arm
-def measure_workload(ds4, layer, wl, steps, warmup, peaks, flush, want_kernels=True) -> dict:
+def measure_workload(ds4, layer, wl, steps, warmup, peaks, flush, want_kernels=True, with_x=False) -> dict:
     inp = synth.make_inputs(wl, device="cuda")
-    x, logits = inp["x"], inp["logits"]
+    x, logits = inp["x"], (None if with_x else inp["logits"])
     out = torch.empty(wl.T, wl.d, dtype=torch.float32, device="cuda")
     for _ in range(warmup):
         if flush:
             flush()
-        layer.forward(x, logits, out)
+        run_forward(layer, x, logits, out)
     torch.cuda.synchronize()
     if layer.status() != ds4.OK:
         raise RuntimeError(f"{wl.name}: device status {ds4.status_string(layer.status())}")
@@ -420,6 +428,29 @@ def run_ours(args):
         if q2k_layer is not None:
             q2k_layer.close()
             torch.cuda.empty_cache()
+        # the whole layer from x: router projection, routed experts, shared expert (fs = 2048, bf16)
+        if layer_wl is base:
+            try:
+                Wx = {**synth.make_layer_weights(base, device="cuda"), **synth.make_dense_weights(base, 2048, device="cuda")}
+                xl = ds4.Layer(base.d, base.E, base.f, base.k, 4096, Wx)
+                del Wx
+                torch.cuda.empty_cache()
+                for name in ("decode1", "decode64", "prefill"):
+                    other = synth.WORKLOADS[name]
+                    fl = L2Flush() if other.T <= 64 else None
+                    r, a, *_ = measure_workload(ds4, xl, other, min(args.steps, 50), args.warmup, peaks, fl,
+                                                with_x=True)
+                    dense_bytes = (base.E * base.d + 3 * 2048 * base.d) * 2
+                    r["algorithmic_bytes"] = a["total_bytes"] - other.T * base.E * 4 + dense_bytes
+                    r["GBps"] = r["algorithmic_bytes"] / (r["ms"] * 1e-3) / 1e9
+                    r["hbm_frac_of_measured"] = r["GBps"] / peaks["hbm_gbs"]
+                    r["note"] = ("x in: router bf16 [256, 4096], routed MXFP4 experts, shared expert bf16 fs = 2048; "
+                                 "bytes: routed weights touched + router + shared weights + x + out")
+                    also[name + "_from_x"] = r
+                xl.close()
+                torch.cuda.empty_cache()
+            except Exception as exc:
+                also["from_x"] = {"error": str(exc)}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0)
     cpu = None

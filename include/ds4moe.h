@@ -106,7 +106,13 @@ enum { DS4MOE_PATH_AUTO = 0, DS4MOE_PATH_DECODE = 1, DS4MOE_PATH_PREFILL = 2, DS
  *                    arrives on, and the GEMM's waits give up after ~1 ms, so
  *                    ds4moe_get_status() reports DS4MOE_ERR_DEVICE_TIMEOUT
  *                    (fault-handling test; no fault, the GPU stays usable).
- *   wait_timeout_ms  bound on every device-side wait (default 2000). */
+ *   wait_timeout_ms  bound on every device-side wait (default 2000).
+ *   has_router       1 = the layer holds a router projection (weights.router)
+ *                    and ds4moe_forward_x computes the logits; 0 = logits are
+ *                    given to ds4moe_forward (default).
+ *   d_ff_shared      intermediate size of one shared expert kept at original
+ *                    precision (bf16 weights), added to every token's output;
+ *                    0 = none (default).  Multiple of 32, at most 16384. */
 typedef struct {
     int32_t d_model, n_experts, d_ff, top_k;
     int32_t max_tokens;
@@ -115,17 +121,25 @@ typedef struct {
     int32_t force_path;
     int32_t debug_fault;
     int32_t wait_timeout_ms;
+    int32_t has_router;
+    int32_t d_ff_shared;
 } ds4moe_config;
 
 /* Canonical weight layout, DEVICE pointers, read only during create.
  *   gate_codes, up_codes   uint8 [E][f][d/2]   MXFP4 codes, row = output unit
  *   gate_scales, up_scales uint8 [E][f][d/32]  E8M0 scales
  *   MXFP4 down: down_codes uint8 [E][d][f/2], down_scales uint8 [E][d][f/32]
- *   Q2_K down:  down_codes uint8 [E][d][f/256][84], down_scales = NULL */
+ *   Q2_K down:  down_codes uint8 [E][d][f/256][84], down_scales = NULL
+ * Original-precision parts (bf16 raw bits; NULL when not configured):
+ *   router       [E][d]      logits = router . x       (has_router = 1)
+ *   shared_gate  [fs][d], shared_up [fs][d], shared_down [d][fs]
+ *                            the shared expert's SwiGLU FFN (d_ff_shared = fs) */
 typedef struct {
     const uint8_t *gate_codes, *gate_scales;
     const uint8_t *up_codes, *up_scales;
     const uint8_t *down_codes, *down_scales;
+    const void *router;
+    const void *shared_gate, *shared_up, *shared_down;
 } ds4moe_weights;
 
 /* Fills *cfg with defaults (all shape fields 0; decode_max_tokens 64,
@@ -153,6 +167,23 @@ int ds4moe_layer_create(const ds4moe_config *cfg, const ds4moe_weights *weights,
  * later through ds4moe_get_status. */
 int ds4moe_forward(ds4moe_layer *layer, const void *x, const float *logits, float *out,
                    int32_t T, ds4moe_stream_t stream);
+
+/* The whole layer from x alone ("DwarfStar実地分析", §GGUFの対応範囲は意図的に
+ * 狭い: the projections, the routing and the shared expert stay at original
+ * precision, the routed experts are quantised): logits = router . x in fp32
+ * (bf16 products, fp32 accumulation), then the routed experts as in
+ * ds4moe_forward, plus the shared expert when d_ff_shared > 0:
+ *   out[t] = sum_j w[t,j] * y[t,j] + Wsd . bf16(silu(Wsg . x) * (Wsu . x)).
+ * The layer must have has_router = 1 (else UNSUPPORTED).  x device bf16
+ * [T][d], out device fp32 [T][d]; asynchronous on `stream`; errors as
+ * ds4moe_forward.  ds4moe_forward itself adds the shared expert too when the
+ * layer has one (its routing then uses the given logits). */
+int ds4moe_forward_x(ds4moe_layer *layer, const void *x, float *out, int32_t T, ds4moe_stream_t stream);
+
+/* Copies the router logits of the most recent ds4moe_forward_x call (device
+ * fp32 [T][E], on `stream`).  Errors: INVALID_ARG (no such call yet, NULL),
+ * CUDA. */
+int ds4moe_get_logits(ds4moe_layer *layer, float *logits, ds4moe_stream_t stream);
 
 /* The same forward pass on HOST buffers: copies x and logits to
  * library-owned device staging on `stream`, runs ds4moe_forward, copies out
@@ -210,6 +241,9 @@ int ds4moe_launches_per_forward(const ds4moe_layer *layer, int32_t T);
  * launch order, and returns how many it wrote (at most max_n), or a negative
  * error.  ds4moe_kernel_name(layer, T, i) names the i-th kernel a forward of
  * T tokens enqueues (NULL past the end):
+ *   A layer with a router or a shared expert first runs dense_in (one cuBLAS
+ *   GEMM: router and shared gate/up rows), and with a shared expert then
+ *   shared_swiglu; after the routed kernels below, shared_down (cuBLAS).
  *   DECODE:                route_topk, route_group, decode_gateup, decode_down
  *   DECODE_MMA, T <= 4:    route_small, decode_mma_gateup, decode_mma_down (gemm_down for Q2_K)
  *   DECODE_MMA, T > 4:     route_topk, route_group, act_quant, decode_mma_gateup, decode_mma_down

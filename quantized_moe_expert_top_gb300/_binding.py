@@ -41,12 +41,15 @@ class Ds4moeError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d_model", "n_experts", "d_ff", "top_k", "max_tokens", "down_format",
-        "decode_max_tokens", "force_path", "debug_fault", "wait_timeout_ms")]
+        "decode_max_tokens", "force_path", "debug_fault", "wait_timeout_ms", "has_router", "d_ff_shared")]
 
 
 class WeightPtrs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales")]
+        "gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales",
+        "router", "shared_gate", "shared_up", "shared_down")]
+
+_DENSE = ("router", "shared_gate", "shared_up", "shared_down")
 
 
 _lib = None
@@ -73,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_layer_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(WeightPtrs), ctypes.POINTER(vp)]
         L.ds4moe_forward.restype = ctypes.c_int
         L.ds4moe_forward.argtypes = [vp, vp, vp, vp, i32, vp]
+        L.ds4moe_forward_x.restype = ctypes.c_int
+        L.ds4moe_forward_x.argtypes = [vp, vp, vp, i32, vp]
+        L.ds4moe_get_logits.restype = ctypes.c_int
+        L.ds4moe_get_logits.argtypes = [vp, vp, vp]
         L.ds4moe_forward_host.restype = ctypes.c_int
         L.ds4moe_forward_host.argtypes = [vp, vp, vp, vp, i32, vp]
         L.ds4moe_get_routing.restype = ctypes.c_int
@@ -144,8 +151,9 @@ class Layer:
     ``weights`` holds the canonical stored tensors on the current CUDA device
     (uint8): gate_codes/up_codes [E,f,d/2], gate_scales/up_scales [E,f,d/32],
     and either down_codes [E,d,f/2] + down_scales [E,d,f/32] (MXFP4) or
-    down_q2k [E,d,f/256,84] (Q2_K).  The library copies them; the caller may
-    free them after construction."""
+    down_q2k [E,d,f/256,84] (Q2_K); optionally, in bf16, router [E,d] and a
+    shared expert shared_gate/shared_up [fs,d], shared_down [d,fs].  The
+    library copies them; the caller may free them after construction."""
 
     def __init__(self, d_model: int, n_experts: int, d_ff: int, top_k: int, max_tokens: int,
                  weights: dict, decode_max_tokens: int = 64, force_path: str = "auto",
@@ -160,11 +168,14 @@ class Layer:
         c.force_path = _PATHS[force_path]
         c.debug_fault = debug_fault
         c.wait_timeout_ms = wait_timeout_ms
+        c.has_router = 1 if weights.get("router") is not None else 0
+        c.d_ff_shared = weights["shared_gate"].shape[0] if weights.get("shared_gate") is not None else 0
         self.cfg = c
         self.down = down
         for name, t in weights.items():
-            if t is not None and (t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous()):
-                raise ValueError(f"weight {name} must be a contiguous uint8 CUDA tensor")
+            want = torch.bfloat16 if name in _DENSE else torch.uint8
+            if t is not None and (t.dtype != want or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"weight {name} must be a contiguous {want} CUDA tensor")
         w = WeightPtrs()
         w.gate_codes = weights["gate_codes"].data_ptr()
         w.gate_scales = weights["gate_scales"].data_ptr()
@@ -176,6 +187,9 @@ class Layer:
         else:
             w.down_codes = weights["down_codes"].data_ptr()
             w.down_scales = weights["down_scales"].data_ptr()
+        for name in _DENSE:
+            if weights.get(name) is not None:
+                setattr(w, name, weights[name].data_ptr())
         h = ctypes.c_void_p()
         rc = lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h))
         if rc != OK:
@@ -197,6 +211,27 @@ class Layer:
             raise Ds4moeError(rc, "ds4moe_forward")
         self._last_T = T
         return out
+
+    def forward_x(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """The layer from x alone: router logits, routed experts, shared expert."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, device=x.device)
+        assert x.dtype == torch.bfloat16 and out.dtype == torch.float32 and x.is_contiguous() and out.is_contiguous()
+        rc = lib().ds4moe_forward_x(self._h, _ptr(x), _ptr(out), T, _stream_handle(stream))
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_forward_x")
+        self._last_T = T
+        return out
+
+    def logits(self, stream=None) -> torch.Tensor:
+        """Router logits of the last forward_x call [T, E] (fp32, device)."""
+        dev = torch.device("cuda", torch.cuda.current_device())
+        r = torch.empty(self._last_T, self.cfg.n_experts, dtype=torch.float32, device=dev)
+        rc = lib().ds4moe_get_logits(self._h, _ptr(r), _stream_handle(stream))
+        if rc != OK:
+            raise Ds4moeError(rc, "ds4moe_get_logits")
+        return r
 
     def forward_host(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
                      stream=None) -> torch.Tensor:
@@ -256,8 +291,8 @@ class Layer:
 
     def kernel_times(self) -> dict:
         """{kernel name: ms} of the most recent forward (timing must be on)."""
-        buf = (ctypes.c_float * 8)()
-        n = lib().ds4moe_kernel_times(self._h, buf, 8)
+        buf = (ctypes.c_float * 12)()
+        n = lib().ds4moe_kernel_times(self._h, buf, 12)
         if n < 0:
             raise Ds4moeError(n, "ds4moe_kernel_times")
         return {lib().ds4moe_kernel_name(self._h, self._last_T, i).decode(): float(buf[i]) for i in range(n)}

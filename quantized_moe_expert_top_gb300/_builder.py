@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libds4moe.so")
-SOURCES = ["layer.cu", "route.cu", "decode.cu", "prefill.cu", "gemm_pair.cu", "decode_mma.cu"]
+SOURCES = ["layer.cu", "route.cu", "decode.cu", "prefill.cu", "gemm_pair.cu", "decode_mma.cu", "dense.cu"]
 HEADERS = ["common.cuh", "gemm.cuh", "internal.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
@@ -52,7 +52,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+    # cuBLAS (the router and shared-expert GEMMs) from the toolkit's library directory
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(NVCC))), "lib64")
+    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-L", cuda_lib, "-lcublas",
+           "-Xlinker", "-rpath," + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

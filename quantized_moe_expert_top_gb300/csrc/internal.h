@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -87,6 +88,9 @@ struct Scratch {
   float* gu_acc;         // [Tdec*k][2f] DECODE_MMA gate/up partial sums (zero between calls)
   int32_t* tile_cnt;     // [E][f/64][dec_maxch] K slices done per gate/up tile and token chunk
   int dec_maxch;         // 128-row token chunks per expert at the DECODE_MMA token limit
+  float* dense_c;        // [Tmax][dense_n] router logits | shared g | shared u (fp32)
+  __nv_bfloat16* h_shared;  // [Tmax][fs] shared-expert h (bf16)
+  void* blas_ws;         // cuBLAS workspace
   uint8_t* stage_x;      // host-call staging: x [Tmax][d] bf16
   float* stage_logits;   // [Tmax][E]
   float* stage_out;      // [Tmax][d]
@@ -139,7 +143,13 @@ struct ds4moe_layer {
   CUtensorMap tm_sfb_x1;  // x scale chunks: 1 row block x 4 K blocks per box
   CUtensorMap tm_sfb_h1;  // h scale chunks, same
   bool decmma_ready;      // the maps above are encoded
-  cudaEvent_t ev[8];   // kernel timing events (created when timing is enabled)
+  void* blas;             // cuBLAS handle (router / shared expert), or null
+  __nv_bfloat16* wcat;    // [dense_n][d] router rows | shared gate rows | shared up rows
+  __nv_bfloat16* wsd;     // [d][fs] shared down
+  int dense_n;            // rows of wcat (E if a router, + 2 fs if a shared expert)
+  int dense_goff;         // column of the first shared gate output in dense_c
+  bool last_forward_x;    // the most recent forward computed its logits
+  cudaEvent_t ev[12];  // kernel timing events (created when timing is enabled)
   bool timing;
   int last_nk;         // kernels in the most recent forward
   int last_T;
@@ -156,13 +166,14 @@ namespace ds4moe {
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; none synchronises.
-cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
+// `lds` = row stride of logits (E, or the dense_in output's width)
+cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, int lds, const void* x, bool prep_x, int T,
                               cudaStream_t st);
 cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream_t st);
 // Few-token routing (T <= kSmallRouteT) in one launch, with the activation
 // quantisation and the zeroing of out when `quant` is set.
-cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const void* x, float* out, int T, int split,
-                               bool quant, cudaStream_t st);
+cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, int lds, const void* x, float* out, int T,
+                               int split, bool quant, cudaStream_t st);
 
 cudaError_t launch_decode_gateup(const ds4moe_layer* L, const void* x, float* out, int T, cudaStream_t st);
 cudaError_t launch_decode_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
@@ -183,6 +194,13 @@ cudaError_t launch_decmma_down(const ds4moe_layer* L, float* out, int T, cudaStr
 // the x (which = 0) or h (which = 1) activations of the last forward.
 cudaError_t launch_gather_act(const ds4moe_layer* L, int which, int T, int split, uint8_t* codes, uint8_t* scales,
                               cudaStream_t st);
+
+// router projection and shared expert (dense.cu, cuBLAS + one kernel)
+cudaError_t launch_dense_in(const ds4moe_layer* L, const void* x, int T, cudaStream_t st);
+cudaError_t launch_shared_swiglu(const ds4moe_layer* L, int T, cudaStream_t st);
+cudaError_t launch_shared_down(const ds4moe_layer* L, float* out, int T, cudaStream_t st);
+cudaError_t dense_create(ds4moe_layer* L, size_t workspace_bytes, void* workspace);
+void dense_destroy(ds4moe_layer* L);
 
 // create-time repacking
 cudaError_t launch_repack_sf(const uint8_t* scales, uint8_t* sf, int E, int rows, int K, int tile_rows, int row_off,

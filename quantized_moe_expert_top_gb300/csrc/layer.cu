@@ -200,6 +200,8 @@ int validate_config(const ds4moe_config* c) {
   if (c->decode_max_tokens < 0) return DS4MOE_ERR_INVALID_ARG;
   if (c->force_path < DS4MOE_PATH_AUTO || c->force_path > DS4MOE_PATH_DECODE_MMA) return DS4MOE_ERR_INVALID_ARG;
   if (c->wait_timeout_ms < 1 || c->wait_timeout_ms > 60000) return DS4MOE_ERR_INVALID_ARG;
+  if (c->has_router != 0 && c->has_router != 1) return DS4MOE_ERR_INVALID_ARG;
+  if (c->d_ff_shared < 0 || c->d_ff_shared > 16384 || c->d_ff_shared % 32) return DS4MOE_ERR_UNSUPPORTED;
   return DS4MOE_OK;
 }
 
@@ -223,10 +225,17 @@ int path_of(const ds4moe_layer* L, int T) {
   return T <= L->cfg.decode_max_tokens ? DS4MOE_PATH_DECODE_MMA : DS4MOE_PATH_PREFILL;
 }
 
-// Names of the kernels one forward of T tokens enqueues, in launch order.
-int kernel_list(const ds4moe_layer* L, int T, const char** names) {
+// Names of the kernels one forward of T tokens enqueues, in launch order
+// (with_x: the call computes its logits from x).
+bool runs_dense_in(const ds4moe_layer* L, bool with_x) {
+  return L->dense_n > 0 && (with_x || L->cfg.d_ff_shared > 0);
+}
+
+int kernel_list(const ds4moe_layer* L, int T, bool with_x, const char** names) {
   int n = 0;
   const int path = path_of(L, T);
+  if (runs_dense_in(L, with_x)) names[n++] = "dense_in";
+  if (L->cfg.d_ff_shared > 0) names[n++] = "shared_swiglu";
   if (path == DS4MOE_PATH_DECODE) {
     for (const char* k : {"route_topk", "route_group", "decode_gateup", "decode_down"}) names[n++] = k;
   } else {
@@ -240,10 +249,12 @@ int kernel_list(const ds4moe_layer* L, int T, const char** names) {
     names[n++] = dm ? "decode_mma_gateup" : "gemm_gateup";
     names[n++] = (dm && !q2k) ? "decode_mma_down" : "gemm_down";
   }
+  if (L->cfg.d_ff_shared > 0) names[n++] = "shared_down";
   return n;
 }
 
 void free_all(ds4moe_layer* L) {
+  dense_destroy(L);
   for (int i = 0; i < L->n_owned; ++i) cudaFree(L->owned[i]);
   L->n_owned = 0;
 }
@@ -280,6 +291,11 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
   if (!wts || !wts->gate_codes || !wts->gate_scales || !wts->up_codes || !wts->up_scales || !wts->down_codes)
     return DS4MOE_ERR_INVALID_ARG;
   if (cfg->down_format == DS4MOE_DOWN_MXFP4 && !wts->down_scales) return DS4MOE_ERR_INVALID_ARG;
+  if (cfg->has_router && (!wts->router || !aligned16(wts->router))) return DS4MOE_ERR_INVALID_ARG;
+  if (cfg->d_ff_shared > 0 && (!wts->shared_gate || !wts->shared_up || !wts->shared_down ||
+                               !aligned16(wts->shared_gate) || !aligned16(wts->shared_up) ||
+                               !aligned16(wts->shared_down)))
+    return DS4MOE_ERR_INVALID_ARG;
   if (!aligned16(wts->gate_codes) || !aligned16(wts->up_codes) || !aligned16(wts->down_codes) ||
       !aligned16(wts->gate_scales) || !aligned16(wts->up_scales) ||
       (wts->down_scales && !aligned16(wts->down_scales)))
@@ -367,6 +383,33 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       } else {
         TRY(alloc(L, &s.hq, (size_t)pad_rows * f));
         TRY(alloc(L, &s.hsf, (size_t)pad_rows * f / 32));
+      }
+    }
+    const int fs = cfg->d_ff_shared;
+    L->dense_n = (cfg->has_router ? E : 0) + 2 * fs;
+    L->dense_goff = cfg->has_router ? E : 0;
+    if (L->dense_n > 0) {
+      constexpr size_t kBlasWs = 32u << 20;
+      TRY(alloc(L, &L->wcat, (size_t)L->dense_n * d * 2));
+      TRY(alloc(L, &s.dense_c, (size_t)Tm * L->dense_n * 4));
+      TRY(alloc(L, &s.blas_ws, kBlasWs));
+      if (fs > 0) {
+        TRY(alloc(L, &L->wsd, (size_t)d * fs * 2));
+        TRY(alloc(L, &s.h_shared, (size_t)Tm * fs * 2));
+      }
+      bool okc = true;
+      if (cfg->has_router)
+        okc = okc && cudaMemcpy(L->wcat, wts->router, (size_t)E * d * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+      if (fs > 0) {
+        okc = okc && cudaMemcpy(L->wcat + (size_t)L->dense_goff * d, wts->shared_gate, (size_t)fs * d * 2,
+                                cudaMemcpyDeviceToDevice) == cudaSuccess;
+        okc = okc && cudaMemcpy(L->wcat + (size_t)(L->dense_goff + fs) * d, wts->shared_up, (size_t)fs * d * 2,
+                                cudaMemcpyDeviceToDevice) == cudaSuccess;
+        okc = okc && cudaMemcpy(L->wsd, wts->shared_down, (size_t)d * fs * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+      }
+      if (!okc || dense_create(L, kBlasWs, s.blas_ws) != cudaSuccess) {
+        rc = DS4MOE_ERR_CUDA;
+        goto fail;
       }
     }
     TRY(alloc(L, &s.stage_x, (size_t)Tm * d * 2));
@@ -487,23 +530,54 @@ int ds4moe_launches_per_forward(const ds4moe_layer* L, int32_t T) {
   const int p = ds4moe_path_for(L, T);
   if (p < 0) return p;
   if (T == 0) return 0;
-  const char* names[8];
-  return kernel_list(L, T, names);
+  const char* names[12];
+  return kernel_list(L, T, L->last_forward_x, names);
 }
+
+namespace {
+// One forward pass; logits == nullptr: computed from x by the router (dense_in).
+int enqueue_forward(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
+                    ds4moe_stream_t stream);
+}  // namespace
 
 int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
                    ds4moe_stream_t stream) {
   if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (!logits && T > 0) return DS4MOE_ERR_INVALID_ARG;
+  return enqueue_forward(L, x, logits, out, T, stream);
+}
+
+int ds4moe_forward_x(ds4moe_layer* L, const void* x, float* out, int32_t T, ds4moe_stream_t stream) {
+  if (!L) return DS4MOE_ERR_INVALID_ARG;
+  if (!L->cfg.has_router) return DS4MOE_ERR_UNSUPPORTED;
+  return enqueue_forward(L, x, nullptr, out, T, stream);
+}
+
+int ds4moe_get_logits(ds4moe_layer* L, float* logits, ds4moe_stream_t stream) {
+  if (!L || !logits || !L->has_forward || !L->last_forward_x) return DS4MOE_ERR_INVALID_ARG;
+  const size_t E = (size_t)L->cfg.n_experts;
+  if (cudaMemcpy2DAsync(logits, E * 4, L->s.dense_c, (size_t)L->dense_n * 4, E * 4, (size_t)L->last_T,
+                        cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  return DS4MOE_OK;
+}
+
+namespace {
+int enqueue_forward(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
+                    ds4moe_stream_t stream) {
   if (T < 0) return DS4MOE_ERR_INVALID_ARG;
   if (T > L->cfg.max_tokens) return DS4MOE_ERR_TOO_MANY_TOKENS;
   if (T == 0) return DS4MOE_OK;
-  if (!x || !logits || !out || !aligned16(x) || !aligned16(logits) || !aligned16(out)) return DS4MOE_ERR_INVALID_ARG;
+  const bool with_x = logits == nullptr;
+  if (!x || !out || !aligned16(x) || !aligned16(out) || (logits && !aligned16(logits))) return DS4MOE_ERR_INVALID_ARG;
   {
     // out may not overlap x or logits (the kernels zero and accumulate into out
     // while x and the logits are still being read)
     const uintptr_t o0 = (uintptr_t)out, o1 = o0 + (uintptr_t)T * L->cfg.d_model * 4;
     const uintptr_t x0 = (uintptr_t)x, x1 = x0 + (uintptr_t)T * L->cfg.d_model * 2;
-    const uintptr_t l0 = (uintptr_t)logits, l1 = l0 + (uintptr_t)T * L->cfg.n_experts * 4;
+    const uintptr_t l0 = (uintptr_t)logits, l1 = logits ? l0 + (uintptr_t)T * L->cfg.n_experts * 4 : l0;
     if ((o0 < x1 && x0 < o1) || (o0 < l1 && l0 < o1)) return DS4MOE_ERR_INVALID_ARG;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -527,17 +601,26 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   };
   cudaError_t e = L->timing ? cudaEventRecord(L->ev[0], st) : cudaSuccess;
   nk = 1;
+  int lds = L->cfg.n_experts;
+  if (runs_dense_in(L, with_x)) {
+    if (e == cudaSuccess) e = mark(launch_dense_in(L, x, T, st));
+    if (with_x) {
+      logits = L->s.dense_c;
+      lds = L->dense_n;
+    }
+  }
+  if (L->cfg.d_ff_shared > 0 && e == cudaSuccess) e = mark(launch_shared_swiglu(L, T, st));
   if (path == DS4MOE_PATH_DECODE) {
-    if (e == cudaSuccess) e = mark(launch_route_topk(L, logits, x, true, T, st));
+    if (e == cudaSuccess) e = mark(launch_route_topk(L, logits, lds, x, true, T, st));
     if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
     if (e == cudaSuccess) e = mark(launch_decode_gateup(L, x, out, T, st));
     if (e == cudaSuccess) e = mark(launch_decode_down(L, out, T, st));
   } else {
     if (T <= kSmallRouteT) {
       // routing and the activations in one launch
-      if (e == cudaSuccess) e = mark(launch_route_small(L, logits, x, out, T, split, true, st));
+      if (e == cudaSuccess) e = mark(launch_route_small(L, logits, lds, x, out, T, split, true, st));
     } else {
-      if (e == cudaSuccess) e = mark(launch_route_topk(L, logits, x, false, T, st));
+      if (e == cudaSuccess) e = mark(launch_route_topk(L, logits, lds, x, false, T, st));
       if (e == cudaSuccess) e = mark(launch_route_group(L, T, split, st));
       if (e == cudaSuccess) e = mark(launch_act_quant(L, x, out, T, split, st));
     }
@@ -551,6 +634,7 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
         e = mark(q2k ? launch_gemm_down_q2k(L, out, T, 1, st) : launch_gemm_down(L, out, T, split, st));
     }
   }
+  if (L->cfg.d_ff_shared > 0 && e == cudaSuccess) e = mark(launch_shared_down(L, out, T, st));
   L->last_nk = nk - 1;
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -559,9 +643,11 @@ int ds4moe_forward(ds4moe_layer* L, const void* x, const float* logits, float* o
   L->last_T = T;
   L->last_path = path;
   L->last_split = split;
+  L->last_forward_x = with_x;
   L->has_forward = true;
   return DS4MOE_OK;
 }
+}  // namespace
 
 int ds4moe_forward_host(ds4moe_layer* L, const void* x, const float* logits, float* out, int32_t T,
                         ds4moe_stream_t stream) {
@@ -652,7 +738,7 @@ int ds4moe_get_status(ds4moe_layer* L) {
 int ds4moe_set_kernel_timing(ds4moe_layer* L, int enable) {
   if (!L) return DS4MOE_ERR_INVALID_ARG;
   if (enable && !L->ev[0]) {
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 12; ++i)
       if (cudaEventCreate(&L->ev[i]) != cudaSuccess) {
         cudaGetLastError();
         return DS4MOE_ERR_CUDA;
@@ -680,14 +766,14 @@ int ds4moe_kernel_times(ds4moe_layer* L, float* ms, int max_n) {
 
 const char* ds4moe_kernel_name(const ds4moe_layer* L, int32_t T, int i) {
   if (!L || T <= 0 || T > L->cfg.max_tokens || i < 0) return nullptr;
-  const char* names[8];
-  const int n = kernel_list(L, T, names);
+  const char* names[12];
+  const int n = kernel_list(L, T, L->last_forward_x, names);
   return i < n ? names[i] : nullptr;
 }
 
 void ds4moe_destroy(ds4moe_layer* L) {
   if (!L) return;
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 12; ++i)
     if (L->ev[i]) cudaEventDestroy(L->ev[i]);
   free_all(L);
   delete L;

@@ -127,7 +127,7 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, 
   }
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int lds, int T, int E, int k,
                                                          int32_t* __restrict__ idx, float* __restrict__ w,
                                                          const __nv_bfloat16* __restrict__ x, int d,
                                                          uint4* __restrict__ xh, float* __restrict__ xsig) {
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
   if (xh != nullptr) prepare_x_f16(x, token, d, xh, xsig, lane);
-  topk_warp(logits + (size_t)token * E, E, k, lane, idx + (size_t)token * k, w + (size_t)token * k);
+  topk_warp(logits + (size_t)token * lds, E, k, lane, idx + (size_t)token * k, w + (size_t)token * k);
 }
 
 // Inclusive scan of one int per thread over a 256-thread block.
@@ -352,7 +352,7 @@ __device__ __forceinline__ void group_warp(const int32_t* idx, int npairs, int E
 // the routed pairs' rows.  So a decode step needs one launch before its GEMMs,
 // and the routing's serial chain overlaps the quantisation.
 __global__ void __launch_bounds__(1024) route_small_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx, float* __restrict__ w,
+    const float* __restrict__ logits, int lds, int T, int E, int k, int32_t* __restrict__ idx, float* __restrict__ w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ pad_offsets,
     int32_t* __restrict__ perm_tok, int32_t* __restrict__ perm_slot, int32_t* __restrict__ inv,
     int32_t* __restrict__ pad_inv, int32_t* __restrict__ pad_pair, int32_t* __restrict__ touched, int split,
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   uint8_t* s_sf = s_dyn + (size_t)T * d * split;
 
   if (wid < T) {
-    topk_warp(logits + (size_t)wid * E, E, k, lane, idx + (size_t)wid * k, w + (size_t)wid * k);
+    topk_warp(logits + (size_t)wid * lds, E, k, lane, idx + (size_t)wid * k, w + (size_t)wid * k);
     // every token's selection is in idx before warp 0 reads it
     if (T > 1) named_bar_sync(1, 32 * T);
     else __syncwarp();
@@ -432,11 +432,11 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 
 }  // namespace
 
-cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, const void* x, bool prep_x, int T,
+cudaError_t launch_route_topk(const ds4moe_layer* L, const float* logits, int lds, const void* x, bool prep_x, int T,
                               cudaStream_t st) {
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
-  return launch_pdl(route_topk_kernel, blocks, 32 * warps_per_block, 0, st, logits, T, L->cfg.n_experts,
+  return launch_pdl(route_topk_kernel, blocks, 32 * warps_per_block, 0, st, logits, lds, T, L->cfg.n_experts,
                     L->cfg.top_k, L->s.topk_idx, L->s.topk_w, static_cast<const __nv_bfloat16*>(x), L->cfg.d_model,
                     prep_x ? reinterpret_cast<uint4*>(L->s.xh) : nullptr, L->s.xsig);
 }
@@ -448,8 +448,8 @@ cudaError_t launch_route_group(const ds4moe_layer* L, int T, int rpp, cudaStream
                     s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, rpp);
 }
 
-cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const void* x, float* out, int T, int split,
-                               bool quant, cudaStream_t st) {
+cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, int lds, const void* x, float* out, int T,
+                               int split, bool quant, cudaStream_t st) {
   const int E = L->cfg.n_experts, k = L->cfg.top_k;
   const Scratch& s = L->s;
   // dynamic shared memory: the MXFP8 codes and scales of the T rows of x
@@ -461,7 +461,7 @@ cudaError_t launch_route_small(const ds4moe_layer* L, const float* logits, const
   });
   if (e != cudaSuccess) return e;
   const size_t smem = quant ? (size_t)T * L->cfg.d_model * split + (size_t)T * (L->cfg.d_model / 32) * split : 0;
-  return launch_pdl(route_small_kernel, 1, 1024, smem, st, logits, T, E, k, s.topk_idx, s.topk_w, s.counts, s.offsets,
+  return launch_pdl(route_small_kernel, 1, 1024, smem, st, logits, lds, T, E, k, s.topk_idx, s.topk_w, s.counts, s.offsets,
                     s.pad_offsets, s.perm_tok, s.perm_slot, s.inv, s.pad_inv, s.pad_pair, s.touched, split,
                     static_cast<const __nv_bfloat16*>(x), L->cfg.d_model, s.xq, s.xsf, (int)(s.pad_rows_max / 128),
                     out, quant ? 1 : 0);
@@ -548,7 +548,7 @@ extern "C" int ds4moe_route_noalloc(const float* logits, int32_t T, int32_t E, i
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int blocks = (T + 7) / 8;
-  route_topk_kernel<<<blocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, nullptr, 0, nullptr, nullptr);
+  route_topk_kernel<<<blocks, 256, 0, st>>>(logits, E, T, E, k, topk_idx, topk_w, nullptr, 0, nullptr, nullptr);
   route_group_kernel<<<E, 256, 0, st>>>(topk_idx, T, E, k, counts, offsets, pad_offsets, perm_tok, perm_slot, inv,
                                         pad_inv, pad_pair, touched, 1);
   if (cudaGetLastError() != cudaSuccess) return DS4MOE_ERR_CUDA;

@@ -48,7 +48,7 @@ import torch
 __all__ = [
     "Workload", "WORKLOADS", "E2M1_GRID",
     "encode_mxfp4", "encode_q2k", "make_logits", "make_x",
-    "make_layer_weights", "make_inputs",
+    "make_layer_weights", "make_dense_weights", "make_inputs",
 ]
 
 # E2M1 magnitudes for codes 0..7 (OCP MX v1.0, FP4 E2M1).
@@ -285,6 +285,22 @@ def make_layer_weights(wl: Workload, device="cpu", experts: Optional[int] = None
             out["down_q2k"][e] = encode_q2k(wd)
         else:
             out["down_codes"][e], out["down_scales"][e] = encode_mxfp4(wd)
+    return out
+
+
+def make_dense_weights(wl: Workload, fs: int, device="cpu", router: bool = True) -> dict:
+    """Original-precision (bf16) parts of the layer: router [E, d] with entries
+    N(0, 1/d) (so that the logits of N(0,1) activations are about N(0, 1)) and
+    a shared expert of intermediate size fs, gate/up [fs, d] and down [d, fs]
+    with entries N(0, 0.02)."""
+    out = {}
+    g = _gen(device, wl.weight_seed, 200)
+    if router:
+        out["router"] = (torch.randn(wl.E, wl.d, generator=g, device=device) / math.sqrt(wl.d)).to(torch.bfloat16)
+    if fs > 0:
+        out["shared_gate"] = (torch.randn(fs, wl.d, generator=g, device=device) * 0.02).to(torch.bfloat16)
+        out["shared_up"] = (torch.randn(fs, wl.d, generator=g, device=device) * 0.02).to(torch.bfloat16)
+        out["shared_down"] = (torch.randn(wl.d, fs, generator=g, device=device) * 0.02).to(torch.bfloat16)
     return out
 
 
