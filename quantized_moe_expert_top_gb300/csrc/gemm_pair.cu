@@ -43,15 +43,19 @@ constexpr int kPStages = 6;     // K = 128 stage slots, loaded and consumed two 
 constexpr int kPBars = kPStages / 2;
 constexpr int kPNMax = 192;     // token columns (N) per chunk, both CTAs together
 constexpr int kPEpiWarps = 8;   // two per tensor-memory lane quarter
-constexpr int kPThreads = 32 * (2 + kPEpiWarps);
+constexpr int kPCpWarp = 2 + kPEpiWarps;  // the leader's scale-factor copies
+constexpr int kPThreads = 32 * (3 + kPEpiWarps);
 constexpr int kPAcc1 = 192;     // column of the second accumulator buffer
 constexpr int kPSfBase = 384;   // scale-factor slots: SFA 4 + SFB 8 columns each
 constexpr int kPSfSlot = 12;
-// Scale-factor slots in tensor memory, one per stage in issue order.  A slot
-// is rewritten (tcgen05.cp) only once the MMAs that read it are known to be
-// complete: the stages kPStages back are done before new ones are loaded.
-constexpr int kPSfSlots = kPStages + 1;
+// Scale-factor slots in tensor memory, two per step (one per K = 128 block)
+// in issue order, so a slot is rewritten kPBars + 1 steps after its last use:
+// the copy thread waits for the MMAs of the step kPBars back (the stage slot
+// it reuses), and MMAs complete in issue order.
+constexpr int kPSfSlots = 2 * (kPBars + 1);
 static_assert(kPAcc1 + kPNMax <= kPSfBase && kPSfBase + kPSfSlots * kPSfSlot <= 512, "tensor memory");
+static_assert(kPNMax / 2 <= 128, "token rows per CTA fit the 3-D token maps");
+constexpr int kPrefetchSteps = 3;  // weight boxes prefetched into L2 ahead of their load
 constexpr int kSfGroup = 4;     // K blocks whose scale factors one pair of TMA loads brings
 constexpr int kSfRing = 3;      // scale-factor groups in shared memory
 static_assert(kSfGroup % 2 == 0, "scale groups start on a step boundary");
@@ -60,6 +64,10 @@ struct PSmem {
   static constexpr int kA = 128 * 128;           // 128 weight rows x 128 K (E2M1 in 8-bit containers)
   static constexpr int kB = (kPNMax / 2) * 128;  // this CTA's half of the token rows
   static constexpr int kStage = kA + kB;
+  // A step (two K = 128 blocks) is one slot pair laid out [A0 A1 | B0 B1]:
+  // each operand arrives in one 3-D TMA box of two K blocks, B1 right after
+  // B0 (nh rows of 128 bytes each).
+  static constexpr int kStep = 2 * kStage;
   // scale-factor group: SFA chunks of 4 K blocks (4 x 512) | SFB [4 K blocks][2 row blocks][512]
   static constexpr int kSfA = kSfGroup * kSfChunk;
   static constexpr int kSfGroupBytes = kSfA + kSfGroup * 2 * kSfChunk;
@@ -69,7 +77,7 @@ struct PSmem {
   static constexpr int kBarOff = kColOff + kPNMax * 8;
   static constexpr int kTotal = kBarOff + 512 + 1024;          // + barriers, + alignment slack
 };
-static_assert(PSmem::kStage % 1024 == 0, "stage alignment");
+static_assert(PSmem::kStage % 1024 == 0 && (PSmem::kB % 2048) == 0, "stage alignment");
 static_assert(PSmem::kTotal <= 227 * 1024, "shared memory");
 
 struct PairArgs {
@@ -255,7 +263,11 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
   uint64_t* acc_empty = acc_full + 2;                                 // [2] leader: both epilogues drained it
   uint64_t* drain = acc_empty + 2;
   uint64_t* never = drain + 1;                                        // fault test: nothing arrives on it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  uint64_t* sf_full = never + 1;                                      // [kSfRing] leader: a scale group landed
+  uint64_t* sf_empty = sf_full + kSfRing;                             // [kSfRing] its copies to TMEM are done
+  uint64_t* cp_done = sf_empty + kSfRing;                             // [kPBars] leader: a step's scales in TMEM
+  uint64_t* cp_drain = cp_done + kPBars;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_ok = abort_flag + 1;
 
@@ -267,9 +279,15 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPBars; ++s) {
-      mbar_init(&full[s], 1);  // the leader's expect_tx; both CTAs' copies count their bytes
+      mbar_init(&full[s], 1);  // the leader's expect_tx; both CTAs' operand copies count their bytes
       mbar_init(&empty[s], 1);
+      mbar_init(&cp_done[s], 1);  // the scale-copy thread's commit once the step's scales are in TMEM
     }
+    for (int g = 0; g < kSfRing; ++g) {
+      mbar_init(&sf_full[g], 1);
+      mbar_init(&sf_empty[g], 1);
+    }
+    mbar_init(cp_drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 2 * kPEpiWarps);
@@ -306,12 +324,26 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
     // steps are at least kPBars steps back and done by then.
     if (lane == 0) {
       PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
+      // L2 prefetch of this CTA's weight box kPrefetchSteps steps ahead of its load
+      PairIter pf{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
+      bool pf_valid = pf.first_chunk();
+      int pf_kb = 0;
+      auto prefetch_next = [&]() {
+        if (!pf_valid) return;
+        tma_prefetch_3d(&tm_a, 0, weight_tile<M>(args, pf.e, pf.pb, rank) * 128, pf_kb);
+        pf_kb += 2;
+        if (pf_kb >= KB) {
+          pf_kb = 0;
+          pf_valid = pf.next();
+        }
+      };
+      for (int i = 0; i < kPrefetchSteps; ++i) prefetch_next();
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);
-      int bar = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_parity = 0;
+      const uint32_t sf_full0 = mapa_shared(smem_u32(sf_full), 0);
+      int bar = 0, sf_slot = 0;
+      uint32_t phase = 0, sf_phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0, sf_issued = 0, sf_parity = 0;
       bool ok = true;
-      int sfg = 0;  // scale-factor groups issued
       for (bool more = it.first_chunk(); more && ok; more = it.next()) {
         const int nh = round32(it.nch) / 2;  // token rows per CTA
         const CUtensorMap* tb = &bmaps.m[nh / 16 - 1];
@@ -320,7 +352,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         const int tile = weight_tile<M>(args, it.e, it.pb, rank);
         // 4-bit unpacking loads count their packed global bytes
         const uint32_t stage_bytes = 2u * (128u * 64u + (uint32_t)nh * 128u);
-        constexpr uint32_t kSfBytes = 2u * S::kSfGroupBytes;
+        constexpr uint32_t kSfBytes = 2u * S::kSfGroupBytes;  // both CTAs' scale groups
         for (int kb = 0; kb < KB; kb += 2) {
           if (!mbar_wait_bounded(&empty[bar], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
@@ -330,19 +362,33 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
           }
           const int nst = KB - kb >= 2 ? 2 : 1;
           const bool sf_load = kb % kSfGroup == 0;  // scale factors of K blocks kb .. kb + 3 (zeros past K)
-          const uint32_t b_cl = full0 + 8u * bar;
-          if (leader) mbar_arrive_expect_tx(&full[bar], stage_bytes * nst + (sf_load ? kSfBytes : 0u));
-          for (int i = 0; i < nst; ++i) {
-            uint8_t* st = smem + (2 * bar + i) * S::kStage;
-            tma_load_2d_pair(st + S::kA, tb, b_cl, (kb + i) * 128, brow);
-            tma_load_2d_pair(st, &tm_a, b_cl, (kb + i) * 128, tile * 128);
-          }
           if (sf_load) {
-            uint8_t* sf = smem + S::kSfOff + (sfg % kSfRing) * S::kSfGroupBytes;
-            ++sfg;
-            tma_load_2d_pair(sf, &tm_sfa, b_cl, 0, (tile * KB + kb) * 2);
-            tma_load_3d_pair(sf + S::kSfA, &tm_sfb, b_cl, 0, (prow / 128) * 2, kb);
+            // the ring slot's previous group has been copied to TMEM (both CTAs)
+            if (!mbar_wait_bounded(&sf_empty[sf_slot], sf_phase ^ 1u, args.budget_ns, abort_flag)) {
+              report_timeout(args.status, kWhereProducerEmpty);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            const uint32_t g_cl = sf_full0 + 8u * sf_slot;
+            if (leader) mbar_arrive_expect_tx(&sf_full[sf_slot], kSfBytes);
+            uint8_t* sf = smem + S::kSfOff + sf_slot * S::kSfGroupBytes;
+            tma_load_2d_pair(sf, &tm_sfa, g_cl, 0, (tile * KB + kb) * 2);
+            tma_load_3d_pair(sf + S::kSfA, &tm_sfb, g_cl, 0, (prow / 128) * 2, kb);
+            sf_issued |= 1u << sf_slot;
+            sf_parity = (sf_parity & ~(1u << sf_slot)) | (sf_phase << sf_slot);
+            if (++sf_slot == kSfRing) {
+              sf_slot = 0;
+              sf_phase ^= 1u;
+            }
           }
+          const uint32_t b_cl = full0 + 8u * bar;
+          // both K blocks in one box per operand (a block past K reads zeros)
+          if (leader) mbar_arrive_expect_tx(&full[bar], stage_bytes * 2);
+          uint8_t* st = smem + bar * S::kStep;
+          tma_load_3d_pair(st + 2 * S::kA, tb, b_cl, 0, brow, kb);
+          tma_load_3d_pair(st, &tm_a, b_cl, 0, tile * 128, kb);
+          prefetch_next();
           issued_mask |= 1u << bar;
           issued_parity = (issued_parity & ~(1u << bar)) | (phase << bar);
           if (++bar == kPBars) {
@@ -352,13 +398,18 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         }
       }
       if (leader) {
-        // The last issued step of every slot has landed (both CTAs' bytes)
-        // before the pair exits: in a normal run these copies are consumed
-        // anyway; after a wait ran out, this is the drain of what is in flight.
+        // The last issued copies of every slot have landed (both CTAs' bytes)
+        // before the pair exits: in a normal run these are consumed anyway;
+        // after a wait ran out, this is the drain of what is in flight.
         for (int b = 0; b < kPBars; ++b)
           if ((issued_mask >> b) & 1u) {
             volatile int no_abort = 0;
             mbar_wait_bounded(&full[b], (issued_parity >> b) & 1u, args.budget_ns, &no_abort);
+          }
+        for (int g = 0; g < kSfRing; ++g)
+          if ((sf_issued >> g) & 1u) {
+            volatile int no_abort = 0;
+            mbar_wait_bounded(&sf_full[g], (sf_parity >> g) & 1u, args.budget_ns, &no_abort);
           }
       }
     }
@@ -367,16 +418,17 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer (leader)
       PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
-      int bar = 0, sfg = -1, chunk = 0;
+      int bar = 0, chunk = 0;
       uint32_t phase = 0, acc_phase = 0, sf_seq = 0;
       bool ok = true;
-      // Descriptors of stage slot 0 and scale group 0; a slot adds its byte
-      // offset / 16 to the start-address field, a K step of 32 elements adds
-      // 32 bytes.
+      // Descriptors of stage slot 0; a slot adds its byte offset / 16 to the
+      // start-address field, a K step of 32 elements adds 32 bytes.  The scale
+      // factors reach tensor memory through the copy thread; this thread
+      // waits once per step (operands landed, then scales copied) and issues
+      // MMAs only, with no memory access in between.
       const uint32_t st0 = smem_u32(smem);
       const uint64_t adesc0 = smem_desc(st0, 16, 1024, 2);
-      const uint64_t bdesc0 = smem_desc(st0 + S::kA, 16, 1024, 2);
-      const uint64_t sfdesc0 = smem_desc(st0 + S::kSfOff, 0, 128, 0);
+      const uint64_t bdesc0 = smem_desc(st0 + 2 * S::kA, 16, 1024, 2);
       static_assert(S::kXchg < (1 << 18), "descriptor address field");
       constexpr uint32_t kSfIdStep = (1u << 4) | (1u << 29);  // next byte of the 32-bit scale word, A and B
       if (args.debug_fault && blockIdx.x == 0) {
@@ -393,7 +445,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       }
       for (bool more = ok && it.first_chunk(); more && ok; more = it.next(), ++chunk) {
         const int N = round32(it.nch);
-        const int nsf = N > 128 ? 2 : 1;
+        const int nh = N / 2;  // token rows per CTA (one B block of a step)
         const int buf = chunk & 1;
         const uint32_t acc = tmem + (uint32_t)(buf ? kPAcc1 : 0);
         const uint32_t idesc0 = idesc_mx(256, N, 0);
@@ -405,34 +457,32 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         acc_phase ^= 1u << buf;
         tc_fence_after();
         for (int kb = 0; kb < KB; kb += 2) {
-          if (!mbar_wait_bounded(&full[bar], phase, args.budget_ns, abort_flag)) {
+          if (!mbar_wait_bounded(&full[bar], phase, args.budget_ns, abort_flag) ||
+              !mbar_wait_bounded(&cp_done[bar], phase, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereMmaFull);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          const int nst = KB - kb >= 2 ? 2 : 1;
-          if (kb % kSfGroup == 0) ++sfg;
-          const uint64_t sd = sfdesc0 + (uint64_t)(((sfg % kSfRing) * S::kSfGroupBytes) >> 4);
-          // scale factors of both stages first, so the second stage's copies
-          // run while the first stage's MMAs do
-          uint32_t slot[2];
-          for (int i = 0; i < nst; ++i) {
-            const int j = (kb + i) % kSfGroup;
-            slot[i] = tmem + kPSfBase + sf_seq * kPSfSlot;
-            sf_seq = sf_seq + 1 == kPSfSlots ? 0 : sf_seq + 1;
-            tc_cp_32x128b_warpx4_pair(slot[i], sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
-            for (int c = 0; c < nsf; ++c)  // SFB: all token columns (both CTAs hold them)
-              tc_cp_32x128b_warpx4_pair(slot[i] + 4 + 4 * c,
-                                        sd + (uint64_t)((S::kSfA + (2 * j + c) * kSfChunk) >> 4));
-          }
-          for (int i = 0; i < nst; ++i) {
-            const uint64_t soff = (uint64_t)((2 * bar + i) * (S::kStage >> 4));
+          tc_fence_after();
+          const bool two = KB - kb >= 2;
+          const uint32_t slot0 = tmem + kPSfBase + sf_seq * kPSfSlot;
+          sf_seq = sf_seq + 1 == kPSfSlots ? 0 : sf_seq + 1;
+          const uint32_t slot1 = tmem + kPSfBase + sf_seq * kPSfSlot;
+          if (two) sf_seq = sf_seq + 1 == kPSfSlots ? 0 : sf_seq + 1;
+          const uint64_t aoff0 = (uint64_t)((bar * S::kStep) >> 4);
+          const uint64_t aoff1 = aoff0 + (uint64_t)(S::kA >> 4);
+          const uint64_t boff0 = aoff0;                          // bdesc0 points at 2 kA of slot 0
+          const uint64_t boff1 = boff0 + (uint64_t)((nh * 128) >> 4);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj)  // K = 32 (32 bytes) per instruction
-              mma_mxf8f6f4_pair(acc, adesc0 + soff + 2 * jj, bdesc0 + soff + 2 * jj,
-                                idesc0 + (uint32_t)jj * kSfIdStep, slot[i], slot[i] + 4,
-                                (kb + i > 0 || jj > 0) ? 1u : 0u);
+          for (int jj = 0; jj < 4; ++jj)  // K = 32 (32 bytes) per instruction
+            mma_mxf8f6f4_pair(acc, adesc0 + aoff0 + 2 * jj, bdesc0 + boff0 + 2 * jj,
+                              idesc0 + (uint32_t)jj * kSfIdStep, slot0, slot0 + 4, (kb > 0 || jj > 0) ? 1u : 0u);
+          if (two) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              mma_mxf8f6f4_pair(acc, adesc0 + aoff1 + 2 * jj, bdesc0 + boff1 + 2 * jj,
+                                idesc0 + (uint32_t)jj * kSfIdStep, slot1, slot1 + 4, 1u);
           }
           tc_commit_pair(&empty[bar], 0x3);
           if (++bar == kPBars) {
@@ -447,6 +497,66 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       tc_commit_pair(drain, 0x1);
       volatile int never = 0;
       mbar_wait_bounded(drain, 0, args.budget_ns, &never);
+    }
+    __syncwarp();
+  } else if (warp == kPCpWarp) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- scale-factor copies (leader)
+      // Per step: wait for the stage slot's previous MMAs (so the tensor-memory
+      // scale slots this step rewrites are no longer read) and, at a new
+      // scale group, for its TMA loads; copy both stages' SFA and SFB chunks
+      // into tensor memory (both CTAs) and commit them to cp_done, on which
+      // the MMA thread waits.  A group's ring slot is released (sf_empty, both
+      // CTAs) once the copies of its last step are done.
+      PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
+      int bar = 0, groups = 0, gslot = 0;
+      uint32_t phase = 0, sf_seq = 0;
+      bool ok = true, have_group = false;
+      const uint64_t sfdesc0 = smem_desc(smem_u32(smem) + S::kSfOff, 0, 128, 0);
+      for (bool more = it.first_chunk(); more && ok; more = it.next()) {
+        const int nsf = round32(it.nch) > 128 ? 2 : 1;
+        for (int kb = 0; kb < KB; kb += 2) {
+          if (!mbar_wait_bounded(&empty[bar], phase ^ 1u, args.budget_ns, abort_flag)) {
+            report_timeout(args.status, kWhereProducerEmpty);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          if (kb % kSfGroup == 0) {
+            if (have_group) tc_commit_pair(&sf_empty[gslot], 0x3);  // the previous group's copies are issued
+            gslot = groups % kSfRing;
+            const uint32_t gphase = (uint32_t)(groups / kSfRing) & 1u;
+            ++groups;
+            have_group = true;
+            if (!mbar_wait_bounded(&sf_full[gslot], gphase, args.budget_ns, abort_flag)) {
+              report_timeout(args.status, kWhereMmaFull);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          const int nst = KB - kb >= 2 ? 2 : 1;
+          const uint64_t sd = sfdesc0 + (uint64_t)((gslot * S::kSfGroupBytes) >> 4);
+          for (int i = 0; i < nst; ++i) {
+            const int j = (kb + i) % kSfGroup;
+            const uint32_t slot = tmem + kPSfBase + sf_seq * kPSfSlot;
+            sf_seq = sf_seq + 1 == kPSfSlots ? 0 : sf_seq + 1;
+            tc_cp_32x128b_warpx4_pair(slot, sd + (uint64_t)(j * (kSfChunk >> 4)));  // SFA: this CTA's rows
+            for (int c = 0; c < nsf; ++c)  // SFB: all token columns (both CTAs hold them)
+              tc_cp_32x128b_warpx4_pair(slot + 4 + 4 * c, sd + (uint64_t)((S::kSfA + (2 * j + c) * kSfChunk) >> 4));
+          }
+          tc_commit_pair(&cp_done[bar], 0x1);
+          if (++bar == kPBars) {
+            bar = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (have_group) tc_commit_pair(&sf_empty[gslot], 0x3);
+      // every copy issued lands before tensor memory is freed
+      tc_commit_pair(cp_drain, 0x1);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(cp_drain, 0, args.budget_ns, &no_abort);
     }
     __syncwarp();
   } else {
@@ -580,8 +690,9 @@ int max_pairs(int num_sms) {
 template <PMode M>
 cudaError_t launch_pair(const ds4moe_layer* L, const CUtensorMap& a, const CUtensorMap& sfa, const CUtensorMap& sfb,
                         const CUtensorMap* b, const PairArgs& args, cudaStream_t st) {
+  // b: the 3-D token-row maps of 16, 32, ..., 128 rows (a CTA holds at most kPNMax / 2 = 96)
   BoxMaps maps;
-  for (int i = 0; i < kNumBoxMaps; ++i) maps.m[i] = b[i];
+  for (int i = 0; i < kNumBoxMaps; ++i) maps.m[i] = b[i < 8 ? i : 7];
   static InitOnce attr_once;
   cudaError_t e = init_once(attr_once, [] {
     return cudaFuncSetAttribute((const void*)pair_gemm_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -638,7 +749,7 @@ cudaError_t launch_gemm_gateup(const ds4moe_layer* L, int T, int split, cudaStre
   a.hq = L->s.hq;
   a.hsf = L->s.hsf;
   a.h16 = (L->cfg.down_format == DS4MOE_DOWN_Q2K) ? L->s.h16 : nullptr;
-  return launch_pair<PMode::GateUp>(L, L->tm_gu, L->tm_sfa_gu, L->tm_sfb_x, L->tm_xq, a, st);
+  return launch_pair<PMode::GateUp>(L, L->tm_gu3, L->tm_sfa_gu, L->tm_sfb_x, L->tm_xq3, a, st);
 }
 
 cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split, cudaStream_t st) {
@@ -648,7 +759,7 @@ cudaError_t launch_gemm_down(const ds4moe_layer* L, float* out, int T, int split
   a.rows_per_expert = L->cfg.d_model;
   a.K = L->cfg.d_ff;
   a.out = out;
-  return launch_pair<PMode::Down>(L, L->tm_down, L->tm_sfa_dn, L->tm_sfb_h, L->tm_hq, a, st);
+  return launch_pair<PMode::Down>(L, L->tm_dn3, L->tm_sfa_dn, L->tm_sfb_h, L->tm_hq3, a, st);
 }
 
 }  // namespace ds4moe

@@ -481,22 +481,23 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
         tm_ok = tm_ok && encode_sf_weights(&L->tm_sfa_dn, w.down_sf, (uint64_t)E * (d / 128) * (f / 128));
         tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h, s.hsf, r128, (uint64_t)f / 128);
       }
-      if (split_ok) {
-        // gate/up side (both down formats), then the MXFP4 down side
-        tm_ok = tm_ok && encode_3d_kblocks(&L->tm_gu3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu,
-                                           (uint64_t)E * f * 2, (uint64_t)d / 128, w.pitch_gu, 64, 128);
+      // 3-D views loading two K = 128 blocks per box (both tensor-core paths):
+      // gate/up side for both down formats, then the MXFP4 down side
+      tm_ok = tm_ok && encode_3d_kblocks(&L->tm_gu3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.gu,
+                                         (uint64_t)E * f * 2, (uint64_t)d / 128, w.pitch_gu, 64, 128);
+      for (int b = 0; b < 8; ++b)
+        tm_ok = tm_ok && encode_3d_kblocks(&L->tm_xq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, pad_rows,
+                                           (uint64_t)d / 128, d, 128, 16u * (uint32_t)(b + 1));
+      if (!q2k) {
+        tm_ok = tm_ok && encode_3d_kblocks(&L->tm_dn3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn,
+                                           (uint64_t)E * d, (uint64_t)f / 128, w.pitch_dn, 64, 128);
         for (int b = 0; b < 8; ++b)
-          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_xq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.xq, pad_rows,
-                                             (uint64_t)d / 128, d, 128, 16u * (uint32_t)(b + 1));
+          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_hq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, pad_rows,
+                                             (uint64_t)f / 128, f, 128, 16u * (uint32_t)(b + 1));
+      }
+      if (split_ok) {
         tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_x1, s.xsf, r128, (uint64_t)d / 128, 1);
-        if (!q2k) {
-          tm_ok = tm_ok && encode_3d_kblocks(&L->tm_dn3, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn,
-                                             (uint64_t)E * d, (uint64_t)f / 128, w.pitch_dn, 64, 128);
-          for (int b = 0; b < 8; ++b)
-            tm_ok = tm_ok && encode_3d_kblocks(&L->tm_hq3[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, pad_rows,
-                                               (uint64_t)f / 128, f, 128, 16u * (uint32_t)(b + 1));
-          tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h1, s.hsf, r128, (uint64_t)f / 128, 1);
-        }
+        if (!q2k) tm_ok = tm_ok && encode_sf_acts(&L->tm_sfb_h1, s.hsf, r128, (uint64_t)f / 128, 1);
         L->decmma_ready = tm_ok;
       }
       if (!tm_ok) {
