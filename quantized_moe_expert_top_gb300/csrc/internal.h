@@ -133,7 +133,7 @@ struct ds4moe_layer {
   CUtensorMap tm_sfb_h;   // h scale chunks, same
   CUtensorMap tm_xq[ds4moe::kNumBoxMaps];   // 8-bit x, boxes 128 B x (16 * (i + 1)) rows
   CUtensorMap tm_hq[ds4moe::kNumBoxMaps];   // 8-bit h
-  CUtensorMap tm_h16[ds4moe::kNumBoxMaps];  // fp16 h, boxes 64 x (16 * (i + 1)) rows
+  CUtensorMap tm_h16[ds4moe::kNumBoxMaps];  // fp16 h as {64, rows, f/64}, boxes {64, 16 * (i + 1), 2}
   // DECODE_MMA (one CTA per SM): 3-D views {128, rows, K/128} that load two
   // K = 128 blocks per box, and activation scale chunks of one row block
   CUtensorMap tm_gu3;     // gate/up weights, box 128 x 128 rows x 2

@@ -146,6 +146,21 @@ bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, void* base, uint64_t inn
 // `pitch` bytes apart and whose K = 128 blocks are `kstride` bytes apart, with
 // a box of 128 elements x box_rows rows x 2 blocks (128-byte swizzle): one load
 // brings two K = 128 blocks as two consecutive [box_rows][128-byte] tiles.
+// fp16 h [rows][f] seen as {64 elements, rows, f / 64 blocks}: one box
+// {64, box_rows, 2} brings two consecutive 64-element (128-byte) blocks of
+// box_rows rows, each block a 128-byte-swizzled [box_rows][128 B] tile.
+bool encode_h16_kpairs(CUtensorMap* tm, void* base, uint64_t rows, uint64_t f, uint32_t box_rows) {
+  PFN_encodeTiled fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, f / 64};
+  cuuint64_t strides[2] = {f * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool encode_3d_kblocks(CUtensorMap* tm, CUtensorMapDataType dt, void* base, uint64_t rows, uint64_t kblocks,
                        uint64_t pitch, uint64_t kstride, uint32_t box_rows) {
   PFN_encodeTiled fn = get_encode_fn();
@@ -468,8 +483,7 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
         if (!q2k)
           tm_ok = tm_ok && encode_2d(&L->tm_hq[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, f, pad_rows, f, 128, rows);
         else
-          tm_ok = tm_ok && encode_2d(&L->tm_h16[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.h16, f, pad_rows,
-                                     (uint64_t)f * 2, 64, rows);
+          tm_ok = tm_ok && encode_h16_kpairs(&L->tm_h16[b], s.h16, pad_rows, f, rows);
       }
       if (!q2k)
         tm_ok = tm_ok && encode_2d(&L->tm_down, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w.dn, f, (uint64_t)E * d,

@@ -5,17 +5,21 @@
 //               the MXFP8 residual), and zeroes out[] for the combine.
 //   q2k down  : "DwarfStar実地分析" §GGUFの対応範囲は意図的に狭い describes the
 //               engine's asymmetric 2-bit scheme with a Q2_K down projection.
-//               Dequantisation warps expand each Q2_K tile to fp16 in shared
-//               memory (w = d*sc*q - dmin*m), and tcgen05.mma kind::f16 with
-//               the weights as M (swap-AB) multiplies it by the fp16 h of the
-//               expert's tokens; the epilogue multiplies by the routing weight
-//               and red-adds into out[t].
+//               Dequantisation warps expand each Q2_K tile to fp16 in tensor
+//               memory (w = d*sc*q - dmin*m, tcgen05.st), and tcgen05.mma
+//               kind::f16 reads it there as the M side (swap-AB) and the fp16
+//               h of the expert's tokens from shared memory; the epilogue
+//               multiplies by the routing weight and red-adds into out[t].
+//               Keeping the weight tile out of shared memory halves that
+//               memory's traffic per step, which bounded the kernel.
 //
 // The Q2_K GEMM is persistent, one CTA per SM: warp 0 issues the TMA loads of
 // h, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 drain the
-// double-buffered accumulator, warps 10..17 dequantise (two threads per weight
-// row), the last warp streams the Q2_K chunks with bulk copies into a ring of
-// kQRaw slots that runs far ahead of the dequantisation.  Every mbarrier wait is bounded; a wait that
+// double-buffered accumulator, warps 10..17 dequantise into tensor memory (two
+// groups of four taking alternate 64-weight steps, one thread per weight row),
+// warps 18 and 19 stream the Q2_K chunks with bulk copies into a ring of kQRaw
+// slots that runs far ahead of the dequantisation, and warp 20 shares the h
+// loads with warp 0.  Every mbarrier wait is bounded; a wait that
 // runs out records DS4MOE_ERR_DEVICE_TIMEOUT in the layer's status word and
 // the CTA drains its in-flight copies and MMAs (again bounded) before it exits.
 #include "gemm.cuh"
@@ -95,30 +99,44 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
 }
 
 // --------------------------------------------------------------- Q2_K down GEMM
-// Tensor memory (512 columns): accumulator buffers at columns 0 and 256.  One
-// pipeline stage covers 64 contraction elements (128 bytes of fp16 per row).
+// Tensor memory (512 columns): accumulator buffers at columns 0 and kQAcc1,
+// the fp16 weight tiles of the stages between them.  One pipeline stage covers
+// kQKs = 128 contraction elements: two 64-element sub-steps, each a Q2_K
+// chunk of the weights and a 128-byte-wide block of h.  Fewer, larger steps
+// halve the barrier hand-offs per weight byte, which bounded the kernel.
 constexpr int kQNMax = 128;      // token columns per chunk
 constexpr int kQStages = 4;
-constexpr int kQRaw = 28;        // slots of the raw Q2_K chunk ring (84 KB of weights in flight)
-constexpr int kQKs = 64;         // fp16 elements per stage
-constexpr int kQDeqWarps = 8;    // two threads per weight row, two 16-weight sub-blocks each
-constexpr int kQEpiWarps = 8;    // two per tensor-memory lane quarter
-constexpr int kQAcc1 = 256;
-constexpr int kQThreads = 64 + 32 * kQEpiWarps + 32 * kQDeqWarps + 32;
-static_assert(kQAcc1 + kQNMax <= 512, "tensor memory");
+constexpr int kQSub = 2;         // 64-element sub-steps per stage
+constexpr int kQKs = 64 * kQSub;  // fp16 elements per stage
+constexpr int kQRaw = 12;        // slots of the raw ring, kQSub Q2_K chunks each (72 KB of weights in flight)
+constexpr int kQASlot0 = 128;    // tensor-memory columns of the fp16 weight tiles: 32 per sub-step
+constexpr int kQDeqWarps = 8;    // kQDeqGroups groups of four: one thread per weight row and step
+constexpr int kQDeqGroups = kQDeqWarps / 4;
+constexpr int kQEpiWarps = 8;    // kQEpiWarps / 4 per tensor-memory lane quarter
+static_assert(kQEpiWarps % 4 == 0, "epilogue warps cover the lane quarters");
+constexpr int kQAcc1 = 384;
+// One thread keeps about one bulk copy per 0.44 us in flight, whatever the
+// copy's size or how many it has outstanding; so the h tiles and the raw
+// chunks are each issued by kQIssuers threads in different warps, taking
+// alternate steps.
+constexpr int kQIssuers = 2;
+constexpr int kQThreads = 64 + 32 * kQEpiWarps + 32 * kQDeqWarps + 32 * (2 * kQIssuers - 1);
+static_assert(kQStages % kQIssuers == 0 && kQRaw % kQIssuers == 0, "an issuer owns fixed slots");
+static_assert(kQNMax <= kQASlot0 && kQASlot0 + 32 * kQSub * kQStages <= kQAcc1 && kQAcc1 + kQNMax <= 512,
+              "tensor memory");
 
 struct QSmem {
-  static constexpr int kA = kBM * 128;       // fp16 weight tile, 128-byte swizzled rows
-  static constexpr int kB = kQNMax * 128;    // fp16 token tile
-  static constexpr int kStage = kA + kB;
-  static constexpr int kRawOff = kQStages * kStage;  // raw Q2_K chunks, kQ2kChunk bytes each
-  static constexpr int kColOff = kRawOff + kQRaw * kQ2kChunk;  // per-column (token, routing weight)
+  static constexpr int kB = kQSub * kQNMax * 128;  // fp16 token tiles [kQSub][N][128 B] (weights in tensor memory)
+  static constexpr int kStage = kB;
+  static constexpr int kRawSlot = kQSub * kQ2kChunk;  // bytes of one raw slot
+  static constexpr int kRawOff = kQStages * kStage;
+  static constexpr int kColOff = kRawOff + kQRaw * kRawSlot;  // per-column (token, routing weight)
   static constexpr int kBarOff = kColOff + kQNMax * 8;
   static constexpr int kTotal = kBarOff + 1024 + 1024;  // barriers (17 + 2 * kQRaw) and flags, alignment slack
 };
 static_assert(QSmem::kStage % 1024 == 0, "stage alignment");
 static_assert(QSmem::kTotal <= 227 * 1024, "shared memory");
-static_assert((17 + 2 * kQRaw) * 8 + 16 <= 1024, "barrier area");
+static_assert((3 * kQStages + 5 + 2 * kQRaw) * 8 + 16 <= 1024, "barrier area");
 
 struct Q2kArgs {
   const uint8_t* q2k;  // tile-major chunks [E][d/128][f/64][3072]
@@ -197,17 +215,17 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(&full[s], 1);  // producer (TMA bytes of h)
       mbar_init(&empty[s], 1);
-      mbar_init(&afull[s], kQDeqWarps);
+      mbar_init(&afull[s], 4);  // the four warps of one dequantising group
     }
     for (int s = 0; s < kQRaw; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kQDeqWarps);
+      mbar_init(&raw_empty[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kQEpiWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 32);  // one commit per lane of the MMA warp
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -222,23 +240,30 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
   pdl_wait();  // the routing tables and h of this forward are complete from here on
   pdl_launch_dependents();
   const int nunits = __ldg(args.touched + args.E) * mb_per_e;
-  constexpr int kHelperWarp = kQThreads / 32 - 1;
   constexpr int kDeqWarp0 = 2 + kQEpiWarps;
+  constexpr int kHelperWarp0 = kDeqWarp0 + kQDeqWarps;  // raw-chunk issuers: warps kHelperWarp0 ..
+  constexpr int kProdWarp1 = kHelperWarp0 + kQIssuers;  // h issuers: warp 0, then kProdWarp1 ..
+  static_assert(kProdWarp1 + kQIssuers - 1 == kQThreads / 32, "warp roles");
+  const bool h_issuer = warp == 0 || warp >= kProdWarp1;
+  const bool raw_issuer = warp >= kHelperWarp0 && warp < kProdWarp1;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (h tiles)
+  if (h_issuer) {
+    // ------------------------------------------------------------ TMA producers (h tiles)
     if (lane == 0) {
+      const int me = warp == 0 ? 0 : warp - kProdWarp1 + 1;  // takes the steps with step % kQIssuers == me
       QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
-      int stage = 0;
-      uint32_t phase = 0;
+      int step = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (bool more = it.first_chunk(); more && ok; more = it.next()) {
         const int N = round16(it.nch);
         const CUtensorMap* tb = &bmaps.m[N / 16 - 1];  // one box of exactly N token rows
         const int prow = __ldg(args.pad_offsets + it.e) / args.rpp + it.t0;  // h row of the chunk's first token
-        const uint32_t bytes = (uint32_t)N * 128u;
-        for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t bytes = (uint32_t)(kQSub * N * 128);
+        for (int kb = 0; kb < KB; ++kb, ++step) {
+          if (step % kQIssuers != me) continue;
+          const int stage = step % kQStages;
+          const uint32_t phase = (uint32_t)(step / kQStages) & 1u;
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
             *abort_flag = 1;
@@ -246,17 +271,13 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
             break;
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(smem + stage * S::kStage + S::kA, tb, &full[stage], kb * kQKs, prow);
+          tma_load_3d(smem + stage * S::kStage, tb, &full[stage], 0, prow, kb * kQSub);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kQStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
       }
       if (*abort_flag) {
-        // every issued stage's copies land before the CTA exits
+        // every stage copy this thread issued lands before the CTA exits
         for (int s = 0; s < kQStages; ++s)
           if ((issued_mask >> s) & 1u) {
             volatile int never = 0;
@@ -267,109 +288,126 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      int chunk = 0;
-      bool ok = true;
-      // descriptors of stage slot 0; a slot adds stage * kStage (16-byte units)
-      const uint32_t st0 = smem_u32(smem);
-      const uint64_t adesc0 = smem_desc(st0, 16, 1024, 2);
-      const uint64_t bdesc0 = smem_desc(st0 + S::kA, 16, 1024, 2);
-      static_assert(kQStages * S::kStage < (1 << 18), "descriptor address field");
-      for (bool more = it.first_chunk(); more && ok; more = it.next(), ++chunk) {
-        const int N = round16(it.nch);
-        const int buf = chunk & 1;
-        const uint32_t acc = tmem + (uint32_t)(buf * kQAcc1);
-        const uint32_t idesc = idesc_f16(kBM, N);
-        if (!mbar_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
+    // The whole warp runs the loop; one elected lane issues each tcgen05 op.
+    QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    int chunk = 0;
+    bool ok = true;
+    // B descriptor of stage slot 0; a slot adds stage * kStage (16-byte units).
+    // A (the dequantised weight tile) is read from tensor memory.
+    const uint32_t st0 = smem_u32(smem);
+    const uint64_t bdesc0 = smem_desc(st0, 16, 1024, 2);
+    static_assert(kQStages * S::kStage < (1 << 18), "descriptor address field");
+    for (bool more = it.first_chunk(); more && ok; more = it.next(), ++chunk) {
+      const int N = round16(it.nch);
+      const int buf = chunk & 1;
+      const uint32_t acc = tmem + (uint32_t)(buf * kQAcc1);
+      const uint32_t idesc = idesc_f16(kBM, N);
+      if (!warp_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
+        if (lane == 0) {
           report_timeout(args.status, kWhereMmaAccEmpty);
           *abort_flag = 1;
-          break;
         }
-        acc_phase ^= 1u << buf;
-        tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag) ||
-              !mbar_wait_bounded(&afull[stage], phase, args.budget_ns, abort_flag)) {
+        break;
+      }
+      acc_phase ^= 1u << buf;
+      tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!warp_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag) ||
+            !warp_wait_bounded(&afull[stage], phase, args.budget_ns, abort_flag)) {
+          if (lane == 0) {
             report_timeout(args.status, kWhereMmaFull);
             *abort_flag = 1;
-            ok = false;
-            break;
           }
-          tc_fence_after();
-          const uint64_t soff = (uint64_t)(stage * (S::kStage >> 4));
-#pragma unroll
-          for (int j = 0; j < 4; ++j)  // K = 16 fp16 (32 bytes) per instruction
-            mma_f16(acc, adesc0 + soff + 2 * j, bdesc0 + soff + 2 * j, idesc, (kb > 0 || j > 0) ? 1u : 0u);
-          tc_commit(&empty[stage]);
-          if (++stage == kQStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc_commit(&acc_full[buf]);
+        tc_fence_after();
+        const uint64_t soff = (uint64_t)(stage * (S::kStage >> 4));
+        const uint32_t a0 = tmem + (uint32_t)(kQASlot0 + 32 * kQSub * stage);
+#pragma unroll
+        for (int u = 0; u < kQSub; ++u)  // sub-step u: the [N][128 B] h block at u * N * 128 bytes
+#pragma unroll
+          for (int j = 0; j < 4; ++j)  // K = 16 fp16 per instruction: 8 tensor-memory columns of A, 32 bytes of B
+            if (elect_one_sync())
+              mma_f16_tmem_a(acc, a0 + 32 * u + 8 * j, bdesc0 + soff + (uint64_t)(u * N * 8 + 2 * j), idesc,
+                             (kb > 0 || u > 0 || j > 0) ? 1u : 0u);
+        if (elect_one_sync()) tc_commit(&empty[stage]);
+        __syncwarp();
+        if (++stage == kQStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      // every MMA issued lands before tensor memory is freed
-      tc_commit(drain);
+      if (!ok) break;
+      if (elect_one_sync()) tc_commit(&acc_full[buf]);
+      __syncwarp();
+    }
+    // every MMA issued lands before tensor memory is freed: each lane commits
+    // (a commit tracks the committing lane's own MMAs) and the barrier takes 32
+    tc_commit(drain);
+    if (lane == 0) {
       volatile int never = 0;
       mbar_wait_bounded(drain, 0, args.budget_ns, &never);
     }
     __syncwarp();
-  } else if (warp == kHelperWarp) {
-    // ------------------------------------------------------------ raw Q2_K chunks, one bulk copy each
+  } else if (raw_issuer) {
+    // ------------------------------------------------------------ raw Q2_K chunks, kQSub per bulk copy
     // The ring runs up to kQRaw steps ahead of the dequantisation, so that many
     // kilobytes of weights are in flight per SM.
     if (lane == 0) {
+      const int me = warp - kHelperWarp0;  // takes the steps with step % kQIssuers == me
       QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
-      int slot = 0;
-      uint32_t phase = 0, issued = 0;
+      int step = 0, last = -1;  // last: the latest step this thread issued
       bool ok = true;
       for (bool more = it.first_chunk(); more && ok; more = it.next()) {
-        const uint8_t* src = args.q2k + (size_t)(it.e * mb_per_e + it.mb) * KB * kQ2kChunk;
-        for (int kb = 0; kb < KB; ++kb) {
+        const uint8_t* src = args.q2k + (size_t)(it.e * mb_per_e + it.mb) * KB * S::kRawSlot;
+        for (int kb = 0; kb < KB; ++kb, ++step) {
+          if (step % kQIssuers != me) continue;
+          const int slot = step % kQRaw;
+          const uint32_t phase = (uint32_t)(step / kQRaw) & 1u;
           if (!mbar_wait_bounded(&raw_empty[slot], phase ^ 1u, args.budget_ns, abort_flag)) {
             report_timeout(args.status, kWhereProducerEmpty);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&raw_full[slot], kQ2kChunk);
-          bulk_load(raw + slot * kQ2kChunk, src + (size_t)kb * kQ2kChunk, kQ2kChunk, &raw_full[slot]);
-          ++issued;
-          if (++slot == kQRaw) {
-            slot = 0;
-            phase ^= 1u;
-          }
+          mbar_arrive_expect_tx(&raw_full[slot], S::kRawSlot);
+          bulk_load(raw + slot * S::kRawSlot, src + (size_t)kb * S::kRawSlot, S::kRawSlot, &raw_full[slot]);
+          last = step;
         }
       }
-      // every issued copy lands before the CTA exits: the last one of each slot
-      for (uint32_t n = 0; n < kQRaw && n < issued; ++n) {
-        const uint32_t seq = issued - 1 - n;  // a copy still possibly in flight
+      // every copy this thread issued lands before the CTA exits: the last one of each of its slots
+      for (int sq = last; sq >= 0 && sq > last - kQRaw; sq -= kQIssuers) {
         volatile int no_abort = 0;
-        mbar_wait_bounded(&raw_full[seq % kQRaw], (seq / kQRaw) & 1u, args.budget_ns, &no_abort);
+        mbar_wait_bounded(&raw_full[sq % kQRaw], (uint32_t)(sq / kQRaw) & 1u, args.budget_ns, &no_abort);
       }
     }
     __syncwarp();
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ Q2_K -> fp16 weight tile
-    const int dt = (warp - kDeqWarp0) * 32 + lane;
-    const int r = dt & 127;   // weight row of the 128-row tile
-    const int half = dt >> 7;  // sub-blocks 2 half, 2 half + 1 of each 64-weight step
+    // Four warps, one per tensor-memory lane quarter (row r = 32 (warp % 4) +
+    // lane), dequantise one 64-weight step; the kQDeqGroups groups take
+    // alternate steps, so that one group's waits and stores overlap another's
+    // arithmetic.
+    const int r = (warp & 3) * 32 + lane;  // weight row of the 128-row tile
+    const int grp = (warp - kDeqWarp0) >> 2;
+    const uint32_t a_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)kQASlot0;
     QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
-    int stage = 0;
-    uint32_t phase = 0;
     bool ok = true;
     const __half2 k1024 = __float2half2_rn(1024.f);
-    int rslot = 0;
-    uint32_t rphase = 0;
+    int step = 0;  // steps of this CTA over all its chunks
     for (bool more = it.first_chunk(); more && ok; more = it.next()) {
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = 0; kb < KB; ++kb, ++step) {
+        if (step % kQDeqGroups != grp) continue;
+        const int stage = step % kQStages, rslot = step % kQRaw;
+        const uint32_t phase = (uint32_t)(step / kQStages) & 1u, rphase = (uint32_t)(step / kQRaw) & 1u;
+        // The A slot is free once the MMAs of the step this slot held before
+        // are done (empty); the h tile (full) is not needed to dequantise.
         uint32_t got = 0;
         if (lane == 0)
-          got = (mbar_wait_bounded(&full[stage], phase, args.budget_ns, abort_flag) &&
+          got = (mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag) &&
                  mbar_wait_bounded(&raw_full[rslot], rphase, args.budget_ns, abort_flag))
                     ? 1u
                     : 0u;
@@ -382,46 +420,39 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
           ok = false;
           break;
         }
-        uint8_t* st = smem + stage * S::kStage;
-        const uint8_t* ch = raw + rslot * kQ2kChunk;
-        const uint2 qv = *reinterpret_cast<const uint2*>(ch + 16 * r + 8 * half);
-        const uint32_t scw = *reinterpret_cast<const uint16_t*>(ch + 2048 + 4 * r + 2 * half);
-        const uint32_t ddw = *reinterpret_cast<const uint32_t*>(ch + 2560 + 4 * r);
-        const float dd = __half2float(__ushort_as_half((unsigned short)(ddw & 0xFFFFu)));
-        const float dm = __half2float(__ushort_as_half((unsigned short)(ddw >> 16)));
-        const uint32_t words[2] = {qv.x, qv.y};
-        uint8_t* arow = st + r * 128;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {  // sub-block sb = 2 half + j: weights 16 sb .. 16 sb + 15 of the step
-          const int sb = 2 * half + j;
-          const uint32_t scb = (scw >> (8 * j)) & 0xFFu;
-          const __half2 a2 = __float2half2_rn(dd * (float)(scb & 15u));
-          const __half2 nb2 = __float2half2_rn(-dm * (float)(scb >> 4));
-          uint32_t P[8];  // P[n] = {w_2n, w_2n+1}: the repacked word holds w_2n at bit 2n, w_2n+1 at bit 16 + 2n
+        for (int u = 0; u < kQSub; ++u) {  // sub-step u: Q2_K chunk u of the slot, tensor-memory columns 32 u ..
+          const uint8_t* ch = raw + rslot * S::kRawSlot + u * kQ2kChunk;
+          const uint4 qv = *reinterpret_cast<const uint4*>(ch + 16 * r);
+          const uint32_t scw = *reinterpret_cast<const uint32_t*>(ch + 2048 + 4 * r);
+          const uint32_t ddw = *reinterpret_cast<const uint32_t*>(ch + 2560 + 4 * r);
+          const float dd = __half2float(__ushort_as_half((unsigned short)(ddw & 0xFFFFu)));
+          const float dm = __half2float(__ushort_as_half((unsigned short)(ddw >> 16)));
+          const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+          uint32_t P[2][16];  // the row's 64 weights of the sub-step, two f16 per word
 #pragma unroll
-          for (int n = 0; n < 8; ++n) {
-            const uint32_t v = ((words[j] >> (2 * n)) & 0x00030003u) | 0x64006400u;  // f16 1024 + q
-            const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&v), k1024);
-            const __half2 w2 = __hfma2(q2, a2, nb2);
-            P[n] = *reinterpret_cast<const uint32_t*>(&w2);
+          for (int sb = 0; sb < 4; ++sb) {  // sub-block sb: weights 16 sb .. 16 sb + 15 of the sub-step
+            const uint32_t scb = (scw >> (8 * sb)) & 0xFFu;
+            const __half2 a2 = __float2half2_rn(dd * (float)(scb & 15u));
+            const __half2 nb2 = __float2half2_rn(-dm * (float)(scb >> 4));
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {  // {w_2n, w_2n+1}: the repacked word holds w_2n at bit 2n, w_2n+1 at 16 + 2n
+              const uint32_t v = ((words[sb] >> (2 * n)) & 0x00030003u) | 0x64006400u;  // f16 1024 + q
+              const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&v), k1024);
+              const __half2 w2 = __hfma2(q2, a2, nb2);
+              P[sb >> 1][8 * (sb & 1) + n] = *reinterpret_cast<const uint32_t*>(&w2);
+            }
           }
-          // 16-byte chunks 2 sb and 2 sb + 1 of the row, 128-byte swizzle
-          *reinterpret_cast<uint4*>(arow + (((2 * sb) ^ (r & 7)) << 4)) = make_uint4(P[0], P[1], P[2], P[3]);
-          *reinterpret_cast<uint4*>(arow + (((2 * sb + 1) ^ (r & 7)) << 4)) = make_uint4(P[4], P[5], P[6], P[7]);
+          const uint32_t col = (uint32_t)(32 * (kQSub * stage + u));
+          tmem_st_32x32b_x16(a_lane + col, P[0]);
+          tmem_st_32x32b_x16(a_lane + col + 16, P[1]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&afull[stage]);
           mbar_arrive(&raw_empty[rslot]);  // this warp's reads of the raw chunk are done
-        }
-        if (++rslot == kQRaw) {
-          rslot = 0;
-          rphase ^= 1u;
-        }
-        if (++stage == kQStages) {
-          stage = 0;
-          phase ^= 1u;
         }
       }
     }
@@ -462,7 +493,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
       tc_fence_after();
       const uint32_t acc = tmem + (uint32_t)(buf * kQAcc1) + lane_base;
       const int m = it.mb * kBM + q * 32 + lane;  // output feature
-      for (int c0 = part * 16; c0 < N; c0 += 32) {
+      for (int c0 = part * 16; c0 < N; c0 += 16 * (kQEpiWarps / 4)) {
         uint32_t r[16];
         tmem_ld_32x32b_x16(acc + (uint32_t)c0, r);
         tmem_ld_wait();
