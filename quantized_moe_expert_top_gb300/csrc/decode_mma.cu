@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kDEpiWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 32);  // one commit per lane of the MMA warp
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&maps.a);
@@ -299,7 +299,9 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform operands); one elected lane
+    // issues each tcgen05 op.
+    {
       DIter it = make_iter();
       int st = 0, gcount = 0, chunk_no = 0;
       uint32_t ph = 0, acc_phase = 0, sf_seq = 0;
@@ -312,18 +314,22 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
         const int buf = chunk_no & 1;
         const uint32_t acc = tmem + (uint32_t)(buf * kDAcc1);
         const uint32_t idesc0 = idesc_mx(128, nbx, 0);
-        if (!mbar_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
-          report_timeout(args.status, kWhereMmaAccEmpty);
-          *abort_flag = 1;
+        if (!warp_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
+          if (lane == 0) {
+            report_timeout(args.status, kWhereMmaAccEmpty);
+            *abort_flag = 1;
+          }
           break;
         }
         acc_phase ^= 1u << buf;
         tc_fence_after();
         int gslot = 0, gkb0 = it.kb0;
         for (int kb = it.kb0; kb < it.kb1; kb += 2) {
-          if (!mbar_wait_bounded(&full[st], ph, args.budget_ns, abort_flag)) {
-            report_timeout(args.status, kWhereMmaFull);
-            *abort_flag = 1;
+          if (!warp_wait_bounded(&full[st], ph, args.budget_ns, abort_flag)) {
+            if (lane == 0) {
+              report_timeout(args.status, kWhereMmaFull);
+              *abort_flag = 1;
+            }
             ok = false;
             break;
           }
@@ -344,11 +350,13 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
           sf_seq = sf_seq + 1 == kDSfSlots ? 0 : sf_seq + 1;
           const uint32_t slot1 = tmem + kDSfBase + sf_seq * kDSfSlot;
           if (two) sf_seq = sf_seq + 1 == kDSfSlots ? 0 : sf_seq + 1;
-          tc_cp_32x128b_warpx4(slot0, smem_desc(sfg + (uint32_t)(j0 * kSfChunk), 0, 128, 0));
-          tc_cp_32x128b_warpx4(slot0 + 4, smem_desc(sfg + (uint32_t)((kDGroup + j0) * kSfChunk), 0, 128, 0));
-          if (two) {
-            tc_cp_32x128b_warpx4(slot1, smem_desc(sfg + (uint32_t)((j0 + 1) * kSfChunk), 0, 128, 0));
-            tc_cp_32x128b_warpx4(slot1 + 4, smem_desc(sfg + (uint32_t)((kDGroup + j0 + 1) * kSfChunk), 0, 128, 0));
+          if (elect_one_sync()) {
+            tc_cp_32x128b_warpx4(slot0, smem_desc(sfg + (uint32_t)(j0 * kSfChunk), 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot0 + 4, smem_desc(sfg + (uint32_t)((kDGroup + j0) * kSfChunk), 0, 128, 0));
+            if (two) {
+              tc_cp_32x128b_warpx4(slot1, smem_desc(sfg + (uint32_t)((j0 + 1) * kSfChunk), 0, 128, 0));
+              tc_cp_32x128b_warpx4(slot1 + 4, smem_desc(sfg + (uint32_t)((kDGroup + j0 + 1) * kSfChunk), 0, 128, 0));
+            }
           }
           const uint64_t ad0 = smem_desc(sa, 16, 1024, 2);
           const uint64_t bd0 = smem_desc(sa + (uint32_t)kDAStage, 16, 1024, 2);
@@ -357,26 +365,35 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_mma_kernel(const __grid_c
           const uint32_t first = kb > it.kb0 ? 1u : 0u;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)  // K = 32 (32 bytes) per instruction
-            mma_mxf8f6f4(acc, ad0 + 2 * jj, bd0 + 2 * jj, idesc0 + (uint32_t)jj * kSfIdStep, slot0, slot0 + 4,
-                         jj > 0 ? 1u : first);
+            if (elect_one_sync())
+              mma_mxf8f6f4(acc, ad0 + 2 * jj, bd0 + 2 * jj, idesc0 + (uint32_t)jj * kSfIdStep, slot0, slot0 + 4,
+                           jj > 0 ? 1u : first);
           if (two) {
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-              mma_mxf8f6f4(acc, ad1 + 2 * jj, bd1 + 2 * jj, idesc0 + (uint32_t)jj * kSfIdStep, slot1, slot1 + 4, 1u);
+              if (elect_one_sync())
+                mma_mxf8f6f4(acc, ad1 + 2 * jj, bd1 + 2 * jj, idesc0 + (uint32_t)jj * kSfIdStep, slot1, slot1 + 4,
+                             1u);
           }
-          tc_commit(&empty[st]);
+          if (elect_one_sync()) tc_commit(&empty[st]);
+          __syncwarp();
           if (++st == nst) {
             st = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&acc_full[buf]);
+        if (elect_one_sync()) tc_commit(&acc_full[buf]);
+        __syncwarp();
       }
-      // every MMA issued lands before tensor memory is freed
+      // every MMA issued lands before tensor memory is freed: each lane
+      // commits (a commit tracks the committing lane's own MMAs), the barrier
+      // takes 32
       tc_commit(drain);
-      volatile int no_abort = 0;
-      mbar_wait_bounded(drain, 0, args.budget_ns, &no_abort);
+      if (lane == 0) {
+        volatile int no_abort = 0;
+        mbar_wait_bounded(drain, 0, args.budget_ns, &no_abort);
+      }
     }
     __syncwarp();
   } else {

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 2 * kPEpiWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 32);  // one commit per lane of the leader's MMA warp
     mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -360,7 +360,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
             ok = false;
             break;
           }
-          const int nst = KB - kb >= 2 ? 2 : 1;
           const bool sf_load = kb % kSfGroup == 0;  // scale factors of K blocks kb .. kb + 3 (zeros past K)
           if (sf_load) {
             // the ring slot's previous group has been copied to TMEM (both CTAs)
@@ -415,8 +414,10 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
+    if (leader) {
       // ---------------------------------------------------------- MMA issuer (leader)
+      // The whole warp runs the loop (warp-uniform operands); one elected
+      // lane issues each tcgen05 op.
       PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
       int bar = 0, chunk = 0;
       uint32_t phase = 0, acc_phase = 0, sf_seq = 0;
@@ -437,9 +438,11 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         // load of both CTAs is still issued normally (at most kPBars steps,
         // since no slot is ever freed), and the producer's drain below waits
         // for all of them on this CTA's full barriers before the pair exits.
-        if (!mbar_wait_bounded(never, 0, args.budget_ns, abort_flag)) {
-          report_timeout(args.status, kWhereMmaFull);
-          *abort_flag = 1;
+        if (!warp_wait_bounded(never, 0, args.budget_ns, abort_flag)) {
+          if (lane == 0) {
+            report_timeout(args.status, kWhereMmaFull);
+            *abort_flag = 1;
+          }
           ok = false;
         }
       }
@@ -449,18 +452,22 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
         const int buf = chunk & 1;
         const uint32_t acc = tmem + (uint32_t)(buf ? kPAcc1 : 0);
         const uint32_t idesc0 = idesc_mx(256, N, 0);
-        if (!mbar_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
-          report_timeout(args.status, kWhereMmaAccEmpty);
-          *abort_flag = 1;
+        if (!warp_wait_bounded(&acc_empty[buf], ((acc_phase >> buf) & 1u) ^ 1u, args.budget_ns, abort_flag)) {
+          if (lane == 0) {
+            report_timeout(args.status, kWhereMmaAccEmpty);
+            *abort_flag = 1;
+          }
           break;
         }
         acc_phase ^= 1u << buf;
         tc_fence_after();
         for (int kb = 0; kb < KB; kb += 2) {
-          if (!mbar_wait_bounded(&full[bar], phase, args.budget_ns, abort_flag) ||
-              !mbar_wait_bounded(&cp_done[bar], phase, args.budget_ns, abort_flag)) {
-            report_timeout(args.status, kWhereMmaFull);
-            *abort_flag = 1;
+          if (!warp_wait_bounded(&full[bar], phase, args.budget_ns, abort_flag) ||
+              !warp_wait_bounded(&cp_done[bar], phase, args.budget_ns, abort_flag)) {
+            if (lane == 0) {
+              report_timeout(args.status, kWhereMmaFull);
+              *abort_flag = 1;
+            }
             ok = false;
             break;
           }
@@ -476,27 +483,35 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
           const uint64_t boff1 = boff0 + (uint64_t)((nh * 128) >> 4);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)  // K = 32 (32 bytes) per instruction
-            mma_mxf8f6f4_pair(acc, adesc0 + aoff0 + 2 * jj, bdesc0 + boff0 + 2 * jj,
-                              idesc0 + (uint32_t)jj * kSfIdStep, slot0, slot0 + 4, (kb > 0 || jj > 0) ? 1u : 0u);
+            if (elect_one_sync())
+              mma_mxf8f6f4_pair(acc, adesc0 + aoff0 + 2 * jj, bdesc0 + boff0 + 2 * jj,
+                                idesc0 + (uint32_t)jj * kSfIdStep, slot0, slot0 + 4, (kb > 0 || jj > 0) ? 1u : 0u);
           if (two) {
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-              mma_mxf8f6f4_pair(acc, adesc0 + aoff1 + 2 * jj, bdesc0 + boff1 + 2 * jj,
-                                idesc0 + (uint32_t)jj * kSfIdStep, slot1, slot1 + 4, 1u);
+              if (elect_one_sync())
+                mma_mxf8f6f4_pair(acc, adesc0 + aoff1 + 2 * jj, bdesc0 + boff1 + 2 * jj,
+                                  idesc0 + (uint32_t)jj * kSfIdStep, slot1, slot1 + 4, 1u);
           }
-          tc_commit_pair(&empty[bar], 0x3);
+          if (elect_one_sync()) tc_commit_pair(&empty[bar], 0x3);
+          __syncwarp();
           if (++bar == kPBars) {
             bar = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair(&acc_full[buf], 0x3);
+        if (elect_one_sync()) tc_commit_pair(&acc_full[buf], 0x3);
+        __syncwarp();
       }
-      // every MMA issued lands before tensor memory is freed
+      // every MMA issued lands before tensor memory is freed: each lane
+      // commits (a commit tracks the committing lane's own MMAs), the barrier
+      // takes 32
       tc_commit_pair(drain, 0x1);
-      volatile int never = 0;
-      mbar_wait_bounded(drain, 0, args.budget_ns, &never);
+      if (lane == 0) {
+        volatile int never = 0;
+        mbar_wait_bounded(drain, 0, args.budget_ns, &never);
+      }
     }
     __syncwarp();
   } else if (warp == kPCpWarp) {

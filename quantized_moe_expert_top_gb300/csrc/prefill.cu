@@ -115,10 +115,8 @@ constexpr int kQDeqGroups = kQDeqWarps / 4;
 constexpr int kQEpiWarps = 8;    // kQEpiWarps / 4 per tensor-memory lane quarter
 static_assert(kQEpiWarps % 4 == 0, "epilogue warps cover the lane quarters");
 constexpr int kQAcc1 = 384;
-// One thread keeps about one bulk copy per 0.44 us in flight, whatever the
-// copy's size or how many it has outstanding; so the h tiles and the raw
-// chunks are each issued by kQIssuers threads in different warps, taking
-// alternate steps.
+// The h tiles and the raw chunks are each issued by kQIssuers threads in
+// different warps, taking alternate steps.
 constexpr int kQIssuers = 2;
 constexpr int kQThreads = 64 + 32 * kQEpiWarps + 32 * kQDeqWarps + 32 * (2 * kQIssuers - 1);
 static_assert(kQStages % kQIssuers == 0 && kQRaw % kQIssuers == 0, "an issuer owns fixed slots");
