@@ -403,13 +403,8 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
         const uint32_t phase = (uint32_t)(step / kQStages) & 1u, rphase = (uint32_t)(step / kQRaw) & 1u;
         // The A slot is free once the MMAs of the step this slot held before
         // are done (empty); the h tile (full) is not needed to dequantise.
-        uint32_t got = 0;
-        if (lane == 0)
-          got = (mbar_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag) &&
-                 mbar_wait_bounded(&raw_full[rslot], rphase, args.budget_ns, abort_flag))
-                    ? 1u
-                    : 0u;
-        got = __shfl_sync(0xffffffffu, got, 0);
+        const bool got = warp_wait_bounded(&empty[stage], phase ^ 1u, args.budget_ns, abort_flag) &&
+                         warp_wait_bounded(&raw_full[rslot], rphase, args.budget_ns, abort_flag);
         if (!got) {
           if (lane == 0) {
             report_timeout(args.status, kWhereMmaFull);

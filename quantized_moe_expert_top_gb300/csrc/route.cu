@@ -59,26 +59,36 @@ __device__ __forceinline__ void prepare_x_f16(const __nv_bfloat16* __restrict__ 
   }
 }
 
+// Order key of a logit: unsigned comparison of keys is the comparison of the
+// values, with -0 taken as +0 and NaN as -inf (outside the layer's domain).
+// Every key is above 0, which marks "no candidate".
+__device__ __forceinline__ uint32_t logit_key(float x) {
+  if (x != x) x = -INFINITY;
+  if (x == 0.f) x = 0.f;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Top-k of one token's logits by one warp (lane l holds entries l, l+32, ...,
 // so a lane's own entries are in increasing index order); lane 0 writes the k
 // expert indices (value desc, index asc) and their softmax weights to idx[0..k)
-// and w[0..k).
+// and w[0..k), and the indices also to sidx[0..k) when sidx is given.  Each of
+// the k rounds takes the warp's largest key with one redux.sync and, among the
+// lanes holding it, the smallest index with a second.
 __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k, int lane,
-                                          int32_t* __restrict__ idx, float* __restrict__ w) {
-
+                                          int32_t* __restrict__ idx, float* __restrict__ w, int* sidx = nullptr) {
   float v[kMaxE / 32];
-  uint32_t taken = 0;  // bit i: entry lane+32i already selected, or beyond E
+  uint32_t key[kMaxE / 32];
 #pragma unroll
   for (int i = 0; i < kMaxE / 32; ++i) {
     const int e = lane + 32 * i;
     float x = -INFINITY;
     if (e < E) {
       x = __ldg(row + e);
-      if (x != x) x = -INFINITY;  // NaN ranks with -inf (outside the layer's domain)
-    } else {
-      taken |= 1u << i;
+      if (x != x) x = -INFINITY;
     }
     v[i] = x;
+    key[i] = e < E ? logit_key(x) : 0u;  // entries beyond E are never candidates
   }
 
   float sel_v[kMaxK];
@@ -86,29 +96,23 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, 
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
     if (j < k) {
+      uint32_t bk = 0;
       float bv = -INFINITY;
-      int be = INT_MAX;  // INT_MAX = no candidate
+      uint32_t be = 0xFFFFFFFFu;
 #pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i) {
-        if (!((taken >> i) & 1u) && (be == INT_MAX || v[i] > bv)) {
+      for (int i = 0; i < kMaxE / 32; ++i)
+        if (key[i] > bk) {  // strict: among equal keys the lane's lower index stays
+          bk = key[i];
           bv = v[i];
-          be = lane + 32 * i;
+          be = (uint32_t)(lane + 32 * i);
         }
-      }
-      // warp arg-max under the total order (valid, value desc, index asc)
+      const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t we = __reduce_min_sync(0xffffffffu, bk == wk ? be : 0xFFFFFFFFu);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const bool better = (oe != INT_MAX) && (be == INT_MAX || ov > bv || (ov == bv && oe < be));
-        if (better) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel_v[j] = bv;
-      sel_e[j] = be;
+      for (int i = 0; i < kMaxE / 32; ++i)  // the winner is taken (unrolled: key stays in registers)
+        if (we == (uint32_t)(lane + 32 * i)) key[i] = 0u;
+      sel_v[j] = __shfl_sync(0xffffffffu, bv, (int)(we & 31u));
+      sel_e[j] = (int)we;
     }
   }
 
@@ -122,6 +126,7 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, 
       if (j < k) {
         idx[j] = sel_e[j];
         w[j] = expf(sel_v[j] - sel_v[0]) / z;
+        if (sidx) sidx[j] = sel_e[j];
       }
     }
   }
@@ -278,54 +283,57 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
 // pairs with the same expert (a token selects an expert at most once, so these
 // are earlier tokens).  The same tables as route_group_kernel, and s_prow[p] =
 // the pair's first padded row.
-__device__ __forceinline__ void group_warp(const int32_t* idx, int npairs, int E, int k, int rpp, int lane,
+__device__ __forceinline__ void group_warp(const int* idx, int npairs, int E, int k, int rpp, int lane,
                                            int32_t* counts, int32_t* offsets, int32_t* pad_offsets, int32_t* perm_tok,
                                            int32_t* perm_slot, int32_t* inv, int32_t* pad_inv, int32_t* pad_pair,
                                            int32_t* touched, int* s_off, int* s_poff, int* s_prow) {
+  // Lane l counts experts 8l .. 8l + 7; one packed inclusive scan of the lane
+  // totals (pairs in bits 0-7, padded rows in bits 8-23, touched experts in
+  // bits 24-31: npairs <= 32 keeps each field in range) gives every lane its
+  // starting offsets.
+  static_assert(kMaxE == 8 * 32, "eight experts per lane");
   const int ep = lane < npairs ? idx[lane] : -1;
-  int cnt[kMaxE / 32];
+  int cnt[8];
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) cnt[i] = 0;
+  for (int j = 0; j < 8; ++j) cnt[j] = 0;
   for (int q = 0; q < npairs; ++q) {
     const int eq = __shfl_sync(0xffffffffu, ep, q);
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) cnt[i] += (eq == lane + 32 * i) ? 1 : 0;
+    for (int j = 0; j < 8; ++j) cnt[j] += (eq == 8 * lane + j) ? 1 : 0;
   }
-  int base_c = 0, base_pc = 0, base_t = 0;
+  uint32_t tot = 0;
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int e = lane + 32 * i;
-    const int c = e < E ? cnt[i] : 0;
-    const int pc = (c * rpp + kPadRows - 1) / kPadRows * kPadRows;
-    const int tf = c > 0 ? 1 : 0;
-    int ic = c, ipc = pc, it = tf;
+  for (int j = 0; j < 8; ++j) {
+    const int c = 8 * lane + j < E ? cnt[j] : 0;
+    cnt[j] = c;
+    tot += (uint32_t)c | ((uint32_t)((c * rpp + kPadRows - 1) / kPadRows * kPadRows) << 8) | ((c > 0 ? 1u : 0u) << 24);
+  }
+  uint32_t incl = tot;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int nc = __shfl_up_sync(0xffffffffu, ic, o), npc = __shfl_up_sync(0xffffffffu, ipc, o),
-                nt = __shfl_up_sync(0xffffffffu, it, o);
-      if (lane >= o) {
-        ic += nc;
-        ipc += npc;
-        it += nt;
-      }
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  uint32_t run = incl - tot;  // this lane's exclusive prefix
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = 8 * lane + j;
+    const int c = cnt[j];
     if (e < E) {
-      const int off = base_c + ic - c, poff = base_pc + ipc - pc;
+      const int off = (int)(run & 0xFFu), poff = (int)((run >> 8) & 0xFFFFu);
       counts[e] = c;
       offsets[e] = off;
       pad_offsets[e] = poff;
       s_off[e] = off;
       s_poff[e] = poff;
-      if (c > 0) touched[base_t + it - 1] = e;
+      if (c > 0) touched[run >> 24] = e;
     }
-    base_c += __shfl_sync(0xffffffffu, ic, 31);
-    base_pc += __shfl_sync(0xffffffffu, ipc, 31);
-    base_t += __shfl_sync(0xffffffffu, it, 31);
+    run += (uint32_t)c | ((uint32_t)((c * rpp + kPadRows - 1) / kPadRows * kPadRows) << 8) | ((c > 0 ? 1u : 0u) << 24);
   }
-  if (lane == 0) {
-    offsets[E] = base_c;
-    pad_offsets[E] = base_pc;
-    touched[E] = base_t;
+  if (lane == 31) {  // totals over all experts
+    offsets[E] = (int)(incl & 0xFFu);
+    pad_offsets[E] = (int)((incl >> 8) & 0xFFFFu);
+    touched[E] = (int)(incl >> 24);
   }
   int r = 0;
   for (int q = 0; q < npairs; ++q) {
@@ -361,6 +369,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   // [T][d/32 blocks][split][32] codes, then [T][d/32][split] scale bytes
   extern __shared__ __align__(16) uint8_t s_dyn[];
   __shared__ int s_prow[kSmallRouteT * kMaxK];
+  __shared__ int s_idx[kSmallRouteT * kMaxK];  // the selections, for the grouping without a global round trip
   __shared__ int s_off[kMaxE], s_poff[kMaxE];
   pdl_wait();
   pdl_launch_dependents();
@@ -371,12 +380,12 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   uint8_t* s_sf = s_dyn + (size_t)T * d * split;
 
   if (wid < T) {
-    topk_warp(logits + (size_t)wid * lds, E, k, lane, idx + (size_t)wid * k, w + (size_t)wid * k);
-    // every token's selection is in idx before warp 0 reads it
+    topk_warp(logits + (size_t)wid * lds, E, k, lane, idx + (size_t)wid * k, w + (size_t)wid * k, s_idx + wid * k);
+    // every token's selection is in s_idx before warp 0 reads it
     if (T > 1) named_bar_sync(1, 32 * T);
     else __syncwarp();
     if (wid == 0)
-      group_warp(idx, npairs, E, k, split, lane, counts, offsets, pad_offsets, perm_tok, perm_slot, inv, pad_inv,
+      group_warp(s_idx, npairs, E, k, split, lane, counts, offsets, pad_offsets, perm_tok, perm_slot, inv, pad_inv,
                  pad_pair, touched, s_off, s_poff, s_prow);
   } else if (quant) {
     const int nthr = (int)blockDim.x - 32 * T;
