@@ -422,20 +422,23 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   if (!quant) return;
   __syncthreads();
 
-  for (int task = tid; task < npairs * nblk; task += blockDim.x) {
-    const int p = task / nblk, cb = task % nblk, tb = (p / k) * nblk + cb;
-    const size_t row = (size_t)s_prow[p];
-    const uint4* src = reinterpret_cast<const uint4*>(s_codes + (size_t)tb * split * 32);
-    uint4* dst = reinterpret_cast<uint4*>(xq + row * d + 32 * (size_t)cb);
-    dst[0] = src[0];
-    dst[1] = src[1];
-    xsf[act_sf_index(row, cb, r128)] = s_sf[tb * split];
-    if (split == 2) {
-      uint4* dlo = reinterpret_cast<uint4*>(xq + (row + 1) * d + 32 * (size_t)cb);
-      dlo[0] = src[2];
-      dlo[1] = src[3];
-      xsf[act_sf_index(row + 1, cb, r128)] = s_sf[tb * split + 1];
-    }
+  // Each routed pair's code row (and its lo row) is written in 16-byte
+  // pieces, consecutive threads taking consecutive pieces, so a warp stores
+  // 512 contiguous bytes; then the row's scales as 32-bit words (four
+  // consecutive 32-element blocks share one word of the scale layout).
+  const int pieces = d / 16, words = nblk / 4;
+  for (int task = tid; task < npairs * split * pieces; task += blockDim.x) {
+    const int p = task / (split * pieces), rem = task % (split * pieces), q = rem / pieces, piece = rem % pieces;
+    const int tb = (p / k) * nblk + piece / 2;
+    const uint4 v = *reinterpret_cast<const uint4*>(s_codes + ((size_t)tb * split + q) * 32 + (piece % 2) * 16);
+    *reinterpret_cast<uint4*>(xq + (size_t)(s_prow[p] + q) * d + 16 * (size_t)piece) = v;
+  }
+  for (int task = tid; task < npairs * split * words; task += blockDim.x) {
+    const int p = task / (split * words), rem = task % (split * words), q = rem / words, g = rem % words;
+    const int tb = (p / k) * nblk + 4 * g;
+    const uint32_t word = (uint32_t)s_sf[tb * split + q] | ((uint32_t)s_sf[(tb + 1) * split + q] << 8) |
+                          ((uint32_t)s_sf[(tb + 2) * split + q] << 16) | ((uint32_t)s_sf[(tb + 3) * split + q] << 24);
+    *reinterpret_cast<uint32_t*>(xsf + act_sf_index((size_t)(s_prow[p] + q), 4 * g, r128)) = word;
   }
 }
 
