@@ -285,7 +285,8 @@ def measure_workload(ds4, layer, wl, steps, warmup, peaks, flush, want_kernels=T
     torch.cuda.synchronize()
     if layer.status() != ds4.OK:
         raise RuntimeError(f"{wl.name}: device status after timing")
-    acc = workload_accounting(wl, routing_counts(wl, logits))
+    # the expert loads: of the given logits, or (from x) of the logits the layer's router produced
+    acc = workload_accounting(wl, routing_counts(wl, logits if logits is not None else layer.logits()))
     ms = statistics.median(per_step)
     res = {"T": wl.T, "ms": ms, "tokens_per_s": wl.T / (ms * 1e-3), "U": acc["U"],
            "GBps": acc["total_bytes"] / (ms * 1e-3) / 1e9,
