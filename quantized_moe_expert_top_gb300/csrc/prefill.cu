@@ -394,7 +394,6 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
     const uint32_t a_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)kQASlot0;
     QIter it{(int)blockIdx.x, nunits, (int)gridDim.x, mb_per_e, 0, 0, 0, 0, 0, args.counts, args.touched};
     bool ok = true;
-    const __half2 k1024 = __float2half2_rn(1024.f);
     int step = 0;  // steps of this CTA over all its chunks
     for (bool more = it.first_chunk(); more && ok; more = it.next()) {
       for (int kb = 0; kb < KB; ++kb, ++step) {
@@ -428,10 +427,19 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
             const uint32_t scb = (scw >> (8 * sb)) & 0xFFu;
             const __half2 a2 = __float2half2_rn(dd * (float)(scb & 15u));
             const __half2 nb2 = __float2half2_rn(-dm * (float)(scb >> 4));
+            // {w_2n, w_2n+1}: the repacked word holds w_2n at bit 2n and w_2n+1 at bit
+            // 16 + 2n.  OR-ing the 2-bit field at mantissa bit 2m into the f16 pattern
+            // of 2^(10 - 2m) gives exactly 2^(10 - 2m) + q, so one mask-and-or (and
+            // one shift per word, for pairs 5..7) extracts a pair without shifting it.
+            const uint32_t hi_word = words[sb] >> 10;
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {  // {w_2n, w_2n+1}: the repacked word holds w_2n at bit 2n, w_2n+1 at 16 + 2n
-              const uint32_t v = ((words[sb] >> (2 * n)) & 0x00030003u) | 0x64006400u;  // f16 1024 + q
-              const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&v), k1024);
+            for (int n = 0; n < 8; ++n) {
+              const int m = n < 5 ? n : n - 5;
+              const uint32_t wq = n < 5 ? words[sb] : hi_word;
+              const uint32_t mag = (uint32_t)(25 - 2 * m) << 10;  // f16 bits of 2^(10 - 2m)
+              const uint32_t v = (wq & (0x00030003u << (2 * m))) | (mag | (mag << 16));
+              const __half2 base = __float2half2_rn((float)(1 << (10 - 2 * m)));
+              const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&v), base);
               const __half2 w2 = __hfma2(q2, a2, nb2);
               P[sb >> 1][8 * (sb & 1) + n] = *reinterpret_cast<const uint32_t*>(&w2);
             }
