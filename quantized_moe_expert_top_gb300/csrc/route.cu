@@ -264,17 +264,43 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t* __restr
   // publish s_off and s_poff)
   int r = block_scan_incl(hits, warp_tot) - hits;
   const int off = s_off, poff = s_poff;
-  for (int pair = p0; pair < p1 && hits > 0; ++pair) {
-    if (__ldg(idx + pair) != e) continue;
-    const int pos = off + r, ppos = poff + r * rpp;
-    perm_tok[pos] = pair / k;
-    perm_slot[pos] = pair % k;
-    inv[pair] = pos;
-    pad_inv[pair] = ppos;
-    for (int q = 0; q < rpp; ++q) pad_pair[ppos + q] = pair;
-    ++r;
-    --hits;
+#define DS4_EMIT_PAIR(PAIR)                                   \
+  do {                                                        \
+    const int pair_ = (PAIR);                                 \
+    const int pos_ = off + r, ppos_ = poff + r * rpp;         \
+    perm_tok[pos_] = pair_ / k;                               \
+    perm_slot[pos_] = pair_ % k;                              \
+    inv[pair_] = pos_;                                        \
+    pad_inv[pair_] = ppos_;                                   \
+    pad_pair[ppos_] = pair_;                                  \
+    if (rpp > 1) pad_pair[ppos_ + 1] = pair_; /* rpp <= 2 */   \
+    ++r;                                                      \
+    --hits;                                                   \
+  } while (0)
+  if ((k % 4) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
+    // second pass with batched loads (four 16-byte loads in flight), so a
+    // thread holding a selection of e does not wait one load latency per pair
+    // up to its last one; selections stay in pair order
+    const int4* v4 = reinterpret_cast<const int4*>(idx + p0);
+    const int n4 = (p1 - p0) / 4;
+    for (int i = 0; i < n4 && hits > 0; i += 4) {
+      int4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = i + u < n4 ? __ldg(v4 + i + u) : make_int4(-1, -1, -1, -1);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pb = p0 + 4 * (i + u);
+        if (v[u].x == e) DS4_EMIT_PAIR(pb);
+        if (v[u].y == e) DS4_EMIT_PAIR(pb + 1);
+        if (v[u].z == e) DS4_EMIT_PAIR(pb + 2);
+        if (v[u].w == e) DS4_EMIT_PAIR(pb + 3);
+      }
+    }
+  } else {
+    for (int pair = p0; pair < p1 && hits > 0; ++pair)
+      if (__ldg(idx + pair) == e) DS4_EMIT_PAIR(pair);
   }
+#undef DS4_EMIT_PAIR
 }
 
 // Grouping of the T*k <= 32 pairs of a few-token call by one warp, without
