@@ -306,6 +306,44 @@ def config_of(wl: synth.Workload, ws: int) -> dict:
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
 
 
+def dominant_roofline(kms: dict, acc: dict, workload: str, peaks: dict, fp8_peak: float, fp4_peak: float):
+    """Roofline of the kernel with the largest live event time: its
+    algorithmic bytes (or FLOP) per launch over its mean time, against the
+    measured HBM peak (or the MXFP8 tensor peak when the launch's FLOP take
+    longer at that peak than its bytes at the HBM peak), with the ncu DRAM
+    traffic of the same launch when a current record exists."""
+    dom = max(kms, key=kms.get) if kms else None
+    bytes_key = {"gemm_gateup": "gemm_gateup_bytes", "gemm_down": "gemm_down_bytes",
+                 "decode_mma_gateup": "decode_gateup_bytes", "decode_mma_down": "decode_down_bytes",
+                 "decode_gateup": "decode_gateup_bytes", "decode_down": "decode_down_bytes"}
+    flops_key = {"gemm_gateup": "flops_gateup", "gemm_down": "flops_down",
+                 "decode_mma_gateup": "flops_gateup", "decode_mma_down": "flops_down",
+                 "decode_gateup": "flops_gateup", "decode_down": "flops_down"}
+    if dom not in bytes_key:
+        return None
+    t = kms[dom] * 1e-3
+    gbs = acc[bytes_key[dom]] / t / 1e9
+    tfl = acc[flops_key[dom]] / t / 1e12
+    hbm_time = acc[bytes_key[dom]] / (peaks["hbm_gbs"] * 1e9)
+    tc_time = acc[flops_key[dom]] / (fp8_peak * 1e12)
+    if dom.startswith("gemm") and tc_time > hbm_time:
+        roofline = {"bound": "tensor", "achieved": tfl, "peak": fp8_peak, "unit": "TFLOP/s", "frac": tfl / fp8_peak}
+    else:
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"]}
+    roofline.update({"kernel": dom, "kernel_ms": kms[dom],
+                     "traffic": measured_traffic(dom, workload),
+                     "implementation_bytes": acc["implementation_bytes"].get(dom),
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                     else "fallback",
+                     "algorithmic_bytes": acc[bytes_key[dom]], "algorithmic_flops": acc[flops_key[dom]]})
+    if dom.startswith("gemm"):
+        roofline["tensor_frac_of_mxf8f6f4_peak"] = tfl / fp8_peak
+        roofline["tensor_frac_of_fp4_peak"] = tfl / fp4_peak
+        roofline["hbm_frac"] = gbs / peaks["hbm_gbs"]
+    return roofline
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -341,36 +379,7 @@ def run_ours(args):
     value = job_value(ws, wl.T, ms_step)
 
     # ---- dominant kernel roofline
-    kms = res["kernels_ms"]
-    dom = max(kms, key=kms.get) if kms else None
-    bytes_key = {"gemm_gateup": "gemm_gateup_bytes", "gemm_down": "gemm_down_bytes",
-                 "decode_mma_gateup": "decode_gateup_bytes", "decode_mma_down": "decode_down_bytes",
-                 "decode_gateup": "decode_gateup_bytes", "decode_down": "decode_down_bytes"}
-    flops_key = {"gemm_gateup": "flops_gateup", "gemm_down": "flops_down",
-                 "decode_mma_gateup": "flops_gateup", "decode_mma_down": "flops_down",
-                 "decode_gateup": "flops_gateup", "decode_down": "flops_down"}
-    roofline = None
-    if dom in bytes_key:
-        t = kms[dom] * 1e-3
-        gbs = acc[bytes_key[dom]] / t / 1e9
-        tfl = acc[flops_key[dom]] / t / 1e12
-        hbm_time = acc[bytes_key[dom]] / (peaks["hbm_gbs"] * 1e9)
-        tc_time = acc[flops_key[dom]] / (fp8_peak * 1e12)
-        if dom.startswith("gemm") and tc_time > hbm_time:
-            roofline = {"bound": "tensor", "achieved": tfl, "peak": fp8_peak, "unit": "TFLOP/s", "frac": tfl / fp8_peak}
-        else:
-            roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / peaks["hbm_gbs"]}
-        roofline.update({"kernel": dom, "kernel_ms": kms[dom],
-                         "traffic": measured_traffic(dom, wl.name),
-                         "implementation_bytes": acc["implementation_bytes"].get(dom),
-                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
-                         else "fallback",
-                         "algorithmic_bytes": acc[bytes_key[dom]], "algorithmic_flops": acc[flops_key[dom]]})
-        if dom.startswith("gemm"):
-            roofline["tensor_frac_of_mxf8f6f4_peak"] = tfl / fp8_peak
-            roofline["tensor_frac_of_fp4_peak"] = tfl / fp4_peak
-            roofline["hbm_frac"] = gbs / peaks["hbm_gbs"]
+    roofline = dominant_roofline(res["kernels_ms"], acc, wl.name, peaks, fp8_peak, fp4_peak)
 
     # ---- end to end through the C ABI with host buffers
     xh = x.cpu().pin_memory()
@@ -422,6 +431,7 @@ def run_ours(args):
                     torch.cuda.empty_cache()
                 also[name] = {k: v for k, v in r.items()}
                 also[name]["algorithmic_bytes"] = a["total_bytes"]
+                also[name]["roofline"] = dominant_roofline(r["kernels_ms"], a, name, peaks, fp8_peak, fp4_peak)
                 if other.T <= 64:
                     also[name]["l2"] = "flushed (512 MB write + read back) before every step"
             except Exception as exc:  # report, do not hide
