@@ -451,20 +451,29 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   // Each routed pair's code row (and its lo row) is written in 16-byte
   // pieces, consecutive threads taking consecutive pieces, so a warp stores
   // 512 contiguous bytes; then the row's scales as 32-bit words (four
-  // consecutive 32-element blocks share one word of the scale layout).
-  const int pieces = d / 16, words = nblk / 4;
-  for (int task = tid; task < npairs * split * pieces; task += blockDim.x) {
-    const int p = task / (split * pieces), rem = task % (split * pieces), q = rem / pieces, piece = rem % pieces;
-    const int tb = (p / k) * nblk + piece / 2;
-    const uint4 v = *reinterpret_cast<const uint4*>(s_codes + ((size_t)tb * split + q) * 32 + (piece % 2) * 16);
-    *reinterpret_cast<uint4*>(xq + (size_t)(s_prow[p] + q) * d + 16 * (size_t)piece) = v;
+  // consecutive 32-element blocks share one word of the scale layout).  A
+  // thread keeps one piece (word) position and walks the rows, so the index
+  // arithmetic is done once, not per store.
+  const int pieces = d / 16, words = nblk / 4, nrows = npairs * split;
+  if (tid < (int)blockDim.x / pieces * pieces) {  // pieces <= 512 divides the rows among whole groups
+    const int piece = tid % pieces, rstep = (int)blockDim.x / pieces;
+    const int cb = piece / 2, half16 = (piece % 2) * 16;
+    for (int rr = tid / pieces; rr < nrows; rr += rstep) {
+      const int p = split == 2 ? rr >> 1 : rr, q = split == 2 ? rr & 1 : 0;
+      const int tb = (p / k) * nblk + cb;
+      const uint4 v = *reinterpret_cast<const uint4*>(s_codes + ((size_t)tb * split + q) * 32 + half16);
+      *reinterpret_cast<uint4*>(xq + (size_t)(s_prow[p] + q) * d + 16 * (size_t)piece) = v;
+    }
   }
-  for (int task = tid; task < npairs * split * words; task += blockDim.x) {
-    const int p = task / (split * words), rem = task % (split * words), q = rem / words, g = rem % words;
-    const int tb = (p / k) * nblk + 4 * g;
-    const uint32_t word = (uint32_t)s_sf[tb * split + q] | ((uint32_t)s_sf[(tb + 1) * split + q] << 8) |
-                          ((uint32_t)s_sf[(tb + 2) * split + q] << 16) | ((uint32_t)s_sf[(tb + 3) * split + q] << 24);
-    *reinterpret_cast<uint32_t*>(xsf + act_sf_index((size_t)(s_prow[p] + q), 4 * g, r128)) = word;
+  if (tid < (int)blockDim.x / words * words) {
+    const int g = tid % words, rstep = (int)blockDim.x / words;
+    for (int rr = tid / words; rr < nrows; rr += rstep) {
+      const int p = split == 2 ? rr >> 1 : rr, q = split == 2 ? rr & 1 : 0;
+      const int tb = (p / k) * nblk + 4 * g;
+      const uint32_t word = (uint32_t)s_sf[tb * split + q] | ((uint32_t)s_sf[(tb + 1) * split + q] << 8) |
+                            ((uint32_t)s_sf[(tb + 2) * split + q] << 16) | ((uint32_t)s_sf[(tb + 3) * split + q] << 24);
+      *reinterpret_cast<uint32_t*>(xsf + act_sf_index((size_t)(s_prow[p] + q), 4 * g, r128)) = word;
+    }
   }
 }
 
