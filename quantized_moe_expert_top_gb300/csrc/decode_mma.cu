@@ -17,10 +17,12 @@
 //
 // Work items are (touched expert, 128-row weight tile, 128-row token chunk,
 // K slice).  The number of K slices S (1, 2, 4 or 8) is chosen on the device
-// from the number of tiles so that every SM gets the same number of items;
-// at one token the gate/up weights of 8 experts are 256 tiles, split four ways
-// over the 152 SMs.  A pipeline stage holds two K = 128 blocks (3-D TMA boxes,
-// one load per operand), so the MMA thread waits once per eight MMAs.
+// from the number of tiles, only where it evens out the items per SM by a
+// quarter or more (at one token the 256 gate/up tiles of 8 experts run
+// unsplit: forced splits of 2, 4 and 8 measured slower).  A pipeline stage
+// holds two K = 128 blocks (3-D TMA boxes, one load per operand), so the MMA
+// warp waits once per eight MMAs; it runs its loop warp-uniformly and one
+// elected lane issues each tcgen05 instruction.
 //
 //   gate/up : a tile is the 64 gate rows and the 64 up rows of 64 features
 //             (the tile-major layout of the layer).  The epilogue adds its

@@ -13,7 +13,7 @@
 // 128 weight rows and half of the token rows in its shared memory, and the
 // leader (rank 0) issues the MMAs for both.  Each weight and token byte is
 // written to and read from shared memory once per pair, which is what bounds a
-// single CTA's tile rate, and the smaller stage leaves room for seven stages.
+// single CTA's tile rate, and the smaller stage leaves room for six stage slots.
 //
 //   gate/up : the pair covers 128 features of one expert; each CTA's 128 rows
 //             are the gate rows then the up rows of its 64 features, so its
@@ -25,13 +25,16 @@
 //             routing weight and red-adds into out[t].
 //
 // Warp roles per CTA (persistent, one CTA per SM): warp 0 issues the TMA
-// loads of both operands and, every fourth stage, of the scale factors of the
-// next four stages; warp 1 allocates tensor memory and, in the leader, issues
-// the MMAs; warps 2..9 drain the accumulators.  All loads are TMA (async
-// proxy), so the tensor core reads them with no proxy fence, and both CTAs'
-// loads complete on the leader's barrier.  The accumulator is double-buffered,
-// so a chunk's epilogue overlaps the next chunk's main loop.  Every wait is bounded; a wait that runs out records
-// DS4MOE_ERR_DEVICE_TIMEOUT in the layer's status word and the CTA winds down.
+// loads of both operands (3-D boxes of two K blocks) and, every fourth K
+// block, of the scale factors of the next four; warp 1 allocates tensor
+// memory and, in the leader, issues the MMAs (the whole warp runs the loop, one
+// elected lane issues); warps 2..9 drain the accumulators; warp 10 copies the
+// scale factors into tensor memory.  All loads are TMA (async proxy), so the
+// tensor core reads them with no proxy fence, and both CTAs' loads complete on
+// the leader's barrier.  The accumulator is double-buffered, so a chunk's
+// epilogue overlaps the next chunk's main loop.  Every wait is bounded; a wait
+// that runs out records DS4MOE_ERR_DEVICE_TIMEOUT in the layer's status word
+// and the CTA winds down.
 #include "gemm.cuh"
 
 namespace ds4moe {
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pair_gemm_kernel(const __grid_co
       // scale slots this step rewrites are no longer read) and, at a new
       // scale group, for its TMA loads; copy both stages' SFA and SFB chunks
       // into tensor memory (both CTAs) and commit them to cp_done, on which
-      // the MMA thread waits.  A group's ring slot is released (sf_empty, both
+      // the MMA warp waits.  A group's ring slot is released (sf_empty, both
       // CTAs) once the copies of its last step are done.
       PairIter it{pair, nunits, npairs, per_e, 0, 0, 0, 0, 0, args.counts, args.touched, args.split};
       int bar = 0, groups = 0, gslot = 0;
