@@ -191,6 +191,21 @@ def test_softmax_two(oracle_lib):
     assert abs(w[0, 0] - g["weights"][0]) < 1e-15 and abs(w[0, 1] - g["weights"][1]) < 1e-15
 
 
+def test_route_signed_zero_and_nan(oracle_lib):
+    """The reading of the pages' routing at its edges: -0 ranks with +0 (a tie,
+    broken by the lower index) and NaN ranks with -inf; worked by hand."""
+    nan, inf = float("nan"), float("inf")
+    logits = np.array([[-0.0, 0.0, nan, -inf, 1.0]], np.float32)
+    idx, w = oracle_lib.route(logits, 5)
+    assert idx.tolist() == [[4, 0, 1, 2, 3]]
+    e1 = math.exp(-1.0)
+    z = 1.0 + 2 * e1
+    assert np.allclose(w[0], [1.0 / z, e1 / z, e1 / z, 0.0, 0.0], rtol=0, atol=1e-15)
+    idx3, w3 = oracle_lib.route(logits, 3)
+    assert idx3.tolist() == [[4, 0, 1]]
+    assert abs(w3.sum() - 1.0) < 1e-15
+
+
 def test_topk_brute_force_with_ties(oracle_lib):
     rng = np.random.default_rng(5)
     T, E, k = 50, 37, 6
