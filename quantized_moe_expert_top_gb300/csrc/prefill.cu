@@ -80,6 +80,44 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
   sw |= __shfl_xor_sync(vmask, sw, 2);
   sw_lo |= __shfl_xor_sync(vmask, sw_lo, 1);
   sw_lo |= __shfl_xor_sync(vmask, sw_lo, 2);
+  if (vmask == 0xffffffffu) {
+    // The warp's 32 blocks are 1 KB of a row: staged in shared memory, they
+    // go out as two 512-byte contiguous stores per routed row (a lane's own
+    // 32 bytes would be two half-sector pieces).
+    __shared__ uint4 stage[8][2][64];  // [warp of the block][hi, lo][16-byte piece]
+    uint4* sh = stage[(threadIdx.x >> 5) & 7][0];
+    uint4* sl = stage[(threadIdx.x >> 5) & 7][1];
+    sh[2 * lane] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    sh[2 * lane + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    if (split == 2) {
+      sl[2 * lane] = make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
+      sl[2 * lane + 1] = make_uint4(packed_lo[4], packed_lo[5], packed_lo[6], packed_lo[7]);
+    }
+    __syncwarp();
+    const uint4 h0 = sh[lane], h1 = sh[32 + lane];
+    uint4 l0 = h0, l1 = h1;
+    if (split == 2) {
+      l0 = sl[lane];
+      l1 = sl[32 + lane];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const size_t r = (size_t)rows[j];
+        uint4* dst = reinterpret_cast<uint4*>(xq + r * d + (size_t)part * 1024);
+        dst[lane] = h0;
+        dst[32 + lane] = h1;
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xsf + act_sf_index(r, c, r128)) = sw;
+        if (split == 2) {
+          uint4* dlo = reinterpret_cast<uint4*>(xq + (r + 1) * d + (size_t)part * 1024);
+          dlo[lane] = l0;
+          dlo[32 + lane] = l1;
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xsf + act_sf_index(r + 1, c, r128)) = sw_lo;
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < k) {

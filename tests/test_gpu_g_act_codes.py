@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 TINY6 = synth.Workload("tiny6", 6, 256, 8, 128, 2, 21, 21, "perm")
 MID = synth.Workload("mid", 70, 512, 8, 384, 2, 22, 22, "zipf")
+WIDE = synth.Workload("wide", 70, 2048, 8, 256, 2, 23, 23, "zipf")  # whole-warp rows: staged 512-byte stores
 
 
 def edge_x(wl: synth.Workload) -> torch.Tensor:
@@ -50,7 +51,7 @@ def oracle_rows(xrow: np.ndarray, split: int):
 
 
 @pytest.mark.parametrize("path", ["prefill", "decode_mma"])
-@pytest.mark.parametrize("wl", [TINY6, MID], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [TINY6, MID, WIDE], ids=lambda w: w.name)
 def test_x_codes_bit_exact_and_output_on_edge_inputs(ds4, wl, path):
     W = synth.make_layer_weights(wl, device="cuda")
     x = edge_x(wl)
