@@ -70,3 +70,37 @@ def test_algorithmic_bytes_follow_the_layer_not_the_implementation():
     assert acc["gemm_down_bytes"] == 256 * 4096 * 2048 * 17 // 32 + 4096 * 4096 * 4
     assert acc["implementation_bytes"]["gemm_gateup"] == 32768 * (4096 + 2048) * 33 // 32
     assert acc["total_bytes"] == 3422552064 + 4096 * 4096 * 2 + 4096 * 256 * 4 + 4096 * 4096 * 4
+
+
+def test_dominant_roofline_picks_the_slowest_kernel_and_its_bound():
+    """The roofline object follows the kernel with the largest live time: its
+    algorithmic bytes over its time against the HBM peak, or its FLOP against
+    the MXFP8 peak when those would take longer at that peak; worked by hand."""
+    import numpy as np
+    import synth
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "source": "measured"}
+    wl = synth.WORKLOADS["decode64"]
+    counts = np.zeros(wl.E, int)
+    counts[:64] = 8                                   # 64 touched experts, 512 pairs
+    acc = bench.workload_accounting(wl, counts)
+    r = bench.dominant_roofline({"decode_mma_gateup": 0.1, "decode_mma_down": 0.05, "route_topk": 0.01},
+                                acc, "no-such-workload", peaks, 4000.0, 12000.0)
+    assert r["kernel"] == "decode_mma_gateup" and r["bound"] == "hbm" and r["traffic"] is None
+    gate_up = 64 * 2 * wl.f * (wl.d // 2 + wl.d // 32)  # gate and up rows of 64 experts: codes + scales
+    assert acc["decode_gateup_bytes"] >= gate_up
+    assert r["achieved"] == pytest.approx(acc["decode_gateup_bytes"] / 0.1e-3 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6000.0)
+    # the prefill chunk's gate/up: 2.3 GB at 6 TB/s (0.39 ms) outlast 1.1 TFLOP at 4 PF (0.27 ms), so it is
+    # HBM-bound; at a 2 PF tensor peak the FLOP (0.55 ms) would bound it instead
+    wl = synth.WORKLOADS["prefill"]
+    acc = bench.workload_accounting(wl, np.full(wl.E, wl.T * wl.k // wl.E))
+    flops = 2 * wl.T * wl.k * wl.d * 2 * wl.f
+    assert acc["flops_gateup"] == flops
+    r = bench.dominant_roofline({"gemm_gateup": 0.5, "gemm_down": 0.3}, acc, "prefill", peaks, 4000.0, 12000.0)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["tensor_frac_of_mxf8f6f4_peak"] == pytest.approx(flops / 0.5e-3 / 1e12 / 4000.0)
+    r = bench.dominant_roofline({"gemm_gateup": 0.5, "gemm_down": 0.3}, acc, "prefill", peaks, 2000.0, 6000.0)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(flops / 0.5e-3 / 1e12)
+    assert r["hbm_frac"] == pytest.approx(acc["gemm_gateup_bytes"] / 0.5e-3 / 1e9 / 6000.0)
+    assert bench.dominant_roofline({}, acc, "prefill", peaks, 4000.0, 12000.0) is None
