@@ -16,7 +16,7 @@
 // The Q2_K GEMM is persistent, one CTA per SM: warp 0 issues the TMA loads of
 // h, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 drain the
 // double-buffered accumulator, warps 10..17 dequantise into tensor memory (two
-// groups of four taking alternate 64-weight steps, one thread per weight row),
+// groups of four taking alternate 128-weight steps, one thread per weight row),
 // warps 18 and 19 stream the Q2_K chunks with bulk copies into a ring of kQRaw
 // slots that runs far ahead of the dequantisation, and warp 20 shares the h
 // loads with warp 0.  Every mbarrier wait is bounded; a wait that
@@ -424,9 +424,9 @@ __global__ void __launch_bounds__(kQThreads, 1) q2k_down_kernel(const __grid_con
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ Q2_K -> fp16 weight tile
     // Four warps, one per tensor-memory lane quarter (row r = 32 (warp % 4) +
-    // lane), dequantise one 64-weight step; the kQDeqGroups groups take
-    // alternate steps, so that one group's waits and stores overlap another's
-    // arithmetic.
+    // lane), dequantise one 128-weight step (two Q2_K chunks); the kQDeqGroups
+    // groups take alternate steps, so that one group's waits and stores overlap
+    // another's arithmetic.
     const int r = (warp & 3) * 32 + lane;  // weight row of the 128-row tile
     const int grp = (warp - kDeqWarp0) >> 2;
     const uint32_t a_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)kQASlot0;
