@@ -81,3 +81,14 @@ def test_create_rejects_null_weights(ds4):
     assert ds4.lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h)) == ds4.ERR_INVALID_ARG
     assert ds4.lib().ds4moe_layer_create(ctypes.byref(c), None, ctypes.byref(h)) == ds4.ERR_INVALID_ARG
     assert ds4.lib().ds4moe_layer_create(ctypes.byref(c), ctypes.byref(w), None) == ds4.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """The product has no CPU fallback: without the compiled library the
+    binding raises instead of computing anything."""
+    import pytest
+    import quantized_moe_expert_top_gb300._binding as B
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libds4moe.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="is missing"):
+        B.lib()
