@@ -26,7 +26,7 @@ _SRC = os.path.join(_HERE, "ds4moe_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
-ACT_EXACT, ACT_MXFP8, ACT_MXFP8_X_ONLY = 0, 1, 2
+ACT_EXACT, ACT_MXFP8, ACT_MXFP8_X_ONLY, ACT_MXFP4 = 0, 1, 2, 3
 DOWN_MXFP4, DOWN_Q2K = 0, 1
 
 _lock = threading.Lock()
@@ -66,6 +66,8 @@ def lib():
             L.ds4o_e4m3_encode.restype = ctypes.c_uint8; L.ds4o_e4m3_encode.argtypes = [d]
             L.ds4o_q2k_weight.restype = d; L.ds4o_q2k_weight.argtypes = [u8p, i]
             L.ds4o_mxfp8.restype = None; L.ds4o_mxfp8.argtypes = [dp, i, u8p, u8p]
+            L.ds4o_e2m1_encode.restype = ctypes.c_uint8; L.ds4o_e2m1_encode.argtypes = [d]
+            L.ds4o_mxfp4_act.restype = None; L.ds4o_mxfp4_act.argtypes = [dp, i, u8p, u8p]
             L.ds4o_route.restype = None; L.ds4o_route.argtypes = [fp, i, i, i, i32p, dp]
             L.ds4o_group.restype = None; L.ds4o_group.argtypes = [i32p, i, i, i, i32p, i32p, i32p, i32p, i32p]
             fwd_args = [i, i, i, i, i, i] + [u8p] * 7 + [u16p, i32p, dp, i, i32p, dp]
@@ -105,6 +107,22 @@ def e4m3_encode(v: float) -> int:
 
 def e4m3_decode(b: int) -> float:
     return lib().ds4o_e4m3_decode(b)
+
+
+def e2m1_encode(v: float) -> int:
+    return int(lib().ds4o_e2m1_encode(float(v)))
+
+
+def mxfp4_act(v: np.ndarray):
+    """MXFP4 of a 1-D fp64 activation vector (len % 32 == 0) -> (codes uint8,
+    one E2M1 code 0..15 per element; scales uint8)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    n = v.size
+    assert n % 32 == 0
+    codes = np.empty(n, np.uint8)
+    scales = np.empty(n // 32, np.uint8)
+    lib().ds4o_mxfp4_act(_p(v, ctypes.c_double), n, _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
+    return codes, scales
 
 
 def q2k_weight(block: np.ndarray, i: int) -> float:

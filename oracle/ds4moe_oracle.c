@@ -40,9 +40,15 @@
  *              in) and then -> MXFP8 along f.
  *   ACT_MXFP8_X_ONLY (prefill path with the Q2_K down projection): x ->
  *              MXFP8, h kept in fp64.
+ *   ACT_MXFP4  (all-FP4 prefill, both MMA operands E2M1): x -> MXFP4 along
+ *              d; h rounded to fp32, then -> MXFP4 along f.
  * MXFP8 block rule (OCP v1.0 conversion): s = floor(log2(amax)) - 8 (E4M3
  * emax = 8), clamped to [-127, 127]; s = 0 when amax = 0; element code =
  * E4M3 round-to-nearest-even of v / 2^s, saturating to +-448.
+ * MXFP4 activation block rule (the same conversion for E2M1): s =
+ * floor(log2(amax)) - 2 (E2M1 emax = 2), clamped, s = 0 for amax = 0; code =
+ * E2M1 round-to-nearest-even of v / 2^s (ties to the even code), saturating
+ * to +-6; a negative value that rounds to zero keeps its sign (code 8).
  *
  * Q2_K-style super-block (256 weights = 16 sub-blocks of 16, 84 bytes):
  * bytes 0..15 scale byte j (low nibble sc_j, high nibble m_j); bytes 16..79
@@ -60,7 +66,7 @@
 #include <omp.h>
 #endif
 
-enum { ACT_EXACT = 0, ACT_MXFP8 = 1, ACT_MXFP8_X_ONLY = 2 };
+enum { ACT_EXACT = 0, ACT_MXFP8 = 1, ACT_MXFP8_X_ONLY = 2, ACT_MXFP4 = 3 };
 enum { DOWN_MXFP4 = 0, DOWN_Q2K = 1 };
 
 /* ------------------------------------------------------------------ */
@@ -161,6 +167,53 @@ static void mxfp8_roundtrip(double *v, int n)
     }
 }
 
+/* value -> E2M1 code (bit 3 sign), round to nearest even code, saturating to +-6. */
+uint8_t ds4o_e2m1_encode(double v)
+{
+    uint8_t sign = (v < 0 || (v == 0 && signbit(v))) ? 0x8 : 0x0;
+    double a = fabs(v);
+    if (a >= 6.0) return sign | 7;
+    if (a < 1.0) {                            /* subnormal step 0.5: codes 0, 1 and 2 (= 1.0) */
+        return sign | (uint8_t)nearbyint(a * 2.0);
+    }
+    int e;
+    frexp(a, &e);
+    e -= 1;                                   /* a = 1.m * 2^e, e in {0, 1, 2} */
+    double m = nearbyint((ldexp(a, -e) - 1.0) * 2.0);   /* 0, 1 or 2 */
+    if (m >= 2.0) { m = 0.0; e += 1; }
+    if (e > 2) return sign | 7;
+    return sign | (uint8_t)(((e + 1) << 1) | (int)m);
+}
+
+/* MXFP4 of one 32-element activation block: returns the E8M0 byte, writes
+ * one E2M1 code (0..15) per element. */
+uint8_t ds4o_mxfp4_act_block(const double *v, uint8_t *codes)
+{
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    int s = 0;
+    if (amax > 0.0) {
+        int e;
+        frexp(amax, &e);          /* floor(log2(amax)) = e - 1 */
+        s = (e - 1) - 2;
+        if (s < -127) s = -127;
+        if (s > 127) s = 127;
+    }
+    for (int i = 0; i < 32; ++i) codes[i] = ds4o_e2m1_encode(ldexp(v[i], -s));
+    return (uint8_t)(s + 127);
+}
+
+/* In-place: replace v[0..n) (n % 32 == 0) by its MXFP4 dequantised value. */
+static void mxfp4_roundtrip(double *v, int n)
+{
+    uint8_t codes[32];
+    for (int b = 0; b < n; b += 32) {
+        uint8_t sb = ds4o_mxfp4_act_block(v + b, codes);
+        double sc = ldexp(1.0, (int)sb - 127);
+        for (int i = 0; i < 32; ++i) v[b + i] = ds4o_e2m1(codes[i]) * sc;
+    }
+}
+
 /* One Q2_K-style weight: super-block pointer, index 0..255. */
 double ds4o_q2k_weight(const uint8_t *sb, int i)
 {
@@ -216,9 +269,10 @@ static void expert_ffn(const ds4o_layer *L, int e, const double *xin, int act_mo
         double u = mxfp4_row_dot(L->up_codes + r * (d / 2), L->up_scales + r * (d / 32), d, xin);
         h[i] = g / (1.0 + exp(-g)) * u;
     }
-    if (act_mode == ACT_MXFP8) {
+    if (act_mode == ACT_MXFP8 || act_mode == ACT_MXFP4) {
         for (int i = 0; i < f; ++i) h[i] = (double)(float)h[i];
-        mxfp8_roundtrip(h, f);
+        if (act_mode == ACT_MXFP8) mxfp8_roundtrip(h, f);
+        else mxfp4_roundtrip(h, f);
     }
     #pragma omp parallel for schedule(static)
     for (int m = 0; m < d; ++m) {
@@ -234,7 +288,8 @@ static void expert_ffn(const ds4o_layer *L, int e, const double *xin, int act_mo
 static void token_input(const ds4o_layer *L, const uint16_t *x_row, int act_mode, double *xin)
 {
     for (int c = 0; c < L->d; ++c) xin[c] = ds4o_bf16(x_row[c]);
-    if (act_mode != ACT_EXACT) mxfp8_roundtrip(xin, L->d);
+    if (act_mode == ACT_MXFP4) mxfp4_roundtrip(xin, L->d);
+    else if (act_mode != ACT_EXACT) mxfp8_roundtrip(xin, L->d);
 }
 
 /* ------------------------------------------------------------------ */
@@ -453,6 +508,11 @@ void ds4o_shared_ffn(int d, int fs, const uint16_t *wg, const uint16_t *wu, cons
 }
 
 /* MXFP8 of n values (n % 32 == 0): codes[n], scales[n/32]. */
+void ds4o_mxfp4_act(const double *v, int n, uint8_t *codes, uint8_t *scales)
+{
+    for (int b = 0; b < n / 32; ++b) scales[b] = ds4o_mxfp4_act_block(v + 32 * b, codes + 32 * b);
+}
+
 void ds4o_mxfp8(const double *v, int n, uint8_t *codes, uint8_t *scales)
 {
     for (int b = 0; b < n / 32; ++b) scales[b] = ds4o_mxfp8_block(v + 32 * b, codes + 32 * b);

@@ -275,7 +275,58 @@ def _torch_mxfp8(v: torch.Tensor) -> torch.Tensor:
     return (q * torch.exp2(s)).reshape(v.shape)
 
 
-@pytest.mark.parametrize("mode", ["exact", "mxfp8", "q2k"])
+_E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_by_search(v: float) -> int:
+    """E2M1 code of v found by searching the eight magnitudes: the nearest one,
+    ties to the even code, saturating at 6; the sign in bit 3."""
+    a = min(abs(v), 6.0)
+    best = min(range(8), key=lambda c: (abs(a - _E2M1_MAGNITUDES[c]), c % 2))
+    return best | (8 if (v < 0 or (v == 0 and math.copysign(1.0, v) < 0)) else 0)
+
+
+def _mxfp4_by_search(v: torch.Tensor) -> torch.Tensor:
+    """MXFP4 round trip of an activation vector, the element rounding by search."""
+    out = []
+    for block in v.reshape(-1, 32).tolist():
+        amax = max(abs(t) for t in block)
+        s = 0 if amax == 0 else max(-127, min(127, (math.frexp(amax)[1] - 1) - 2))
+        for t in block:
+            c = _e2m1_by_search(math.ldexp(t, -s))
+            out.append((-1.0 if c & 8 else 1.0) * _E2M1_MAGNITUDES[c & 7] * 2.0 ** s)
+    return torch.tensor(out, dtype=torch.float64).reshape(v.shape)
+
+
+def test_e2m1_encode_hand_values(oracle_lib):
+    """Round to nearest, ties to the even code (OCP MX v1.0 conversion), worked by hand."""
+    cases = [(0.0, 0), (0.25, 0), (0.26, 1), (0.5, 1), (0.75, 2), (1.0, 2), (1.25, 2), (1.3, 3), (1.75, 4),
+             (2.5, 4), (2.6, 5), (3.5, 6), (5.0, 6), (5.5, 7), (6.0, 7), (100.0, 7), (-3.0, 0xD), (-0.2, 0x8)]
+    for v, code in cases:
+        assert oracle_lib.e2m1_encode(v) == code, v
+    for c in range(16):  # every code value encodes to itself (-0 keeps its sign)
+        val = (-1.0 if c & 8 else 1.0) * _E2M1_MAGNITUDES[c & 7]
+        assert oracle_lib.e2m1_encode(val if c != 8 else -0.0) == c
+
+
+def test_e2m1_encode_matches_search(oracle_lib):
+    rng = np.random.default_rng(9)
+    vals = np.concatenate([rng.uniform(-7, 7, 4000), np.array([k / 4 for k in range(-28, 29)])])
+    for v in vals:
+        assert oracle_lib.e2m1_encode(float(v)) == _e2m1_by_search(float(v)), v
+
+
+def test_mxfp4_activation_block_hand(oracle_lib):
+    """amax 0.3: floor(log2 0.3) = -2, s = -4 (scale byte 123); 0.3 * 16 = 4.8 -> 4 (code 6), 0.1 * 16 = 1.6
+    -> 1.5 (code 3), -0.02 * 16 = -0.32 -> -0.5 (code 9); an all-zero block has scale byte 127."""
+    v = np.zeros(64)
+    v[0], v[1], v[2] = 0.3, 0.1, -0.02
+    codes, scales = oracle_lib.mxfp4_act(v)
+    assert scales.tolist() == [123, 127]
+    assert codes[:3].tolist() == [6, 3, 9] and not codes[3:].any()
+
+
+@pytest.mark.parametrize("mode", ["exact", "mxfp8", "q2k", "mxfp4"])
 def test_single_expert_matches_torch_float64(oracle_lib, mode):
     import oracle
     d, f = 256, 256
@@ -283,20 +334,22 @@ def test_single_expert_matches_torch_float64(oracle_lib, mode):
     W = _np_weights(synth.make_layer_weights(wl))
     x = synth.make_x(wl)
     dims = _dims(d, 1, f, 1)
-    act = {"exact": oracle.ACT_EXACT, "mxfp8": oracle.ACT_MXFP8, "q2k": oracle.ACT_MXFP8_X_ONLY}[mode]
+    act = {"exact": oracle.ACT_EXACT, "mxfp8": oracle.ACT_MXFP8, "q2k": oracle.ACT_MXFP8_X_ONLY,
+           "mxfp4": oracle.ACT_MXFP4}[mode]
     out = oracle_lib.forward(dims, W, _bits(x), np.zeros((3, 1), np.int32), np.ones((3, 1)), [0, 1, 2], act)
     wg, wu, wd = (torch.from_numpy(a) for a in oracle_lib.dequant_expert(dims, W, 0))
     xx = x.to(torch.float64)
+    rt = _mxfp4_by_search if mode == "mxfp4" else _torch_mxfp8
     if mode != "exact":
-        xx = torch.stack([_torch_mxfp8(r) for r in xx])
+        xx = torch.stack([rt(r) for r in xx])
     h = torch.nn.functional.silu(xx @ wg.T) * (xx @ wu.T)
-    if mode == "mxfp8":
-        h = torch.stack([_torch_mxfp8(r.to(torch.float32).to(torch.float64)) for r in h])
+    if mode in ("mxfp8", "mxfp4"):
+        h = torch.stack([rt(r.to(torch.float32).to(torch.float64)) for r in h])
     ref = h @ wd.T
     assert np.allclose(out, ref.numpy(), rtol=1e-12, atol=1e-14 * float(ref.abs().max()))
 
 
-@pytest.mark.parametrize("act", [0, 1, 2])
+@pytest.mark.parametrize("act", [0, 1, 2, 3])
 def test_routed_equals_dense_mask(oracle_lib, act):
     wl = synth.WORKLOADS["tiny"]
     if act == 2:
