@@ -88,7 +88,7 @@ struct Scratch {
   float* gu_acc;         // [Tdec*k][2f] DECODE_MMA gate/up partial sums (zero between calls)
   int32_t* tile_cnt;     // [E][f/64][dec_maxch] K slices done per gate/up tile and token chunk
   int dec_maxch;         // 128-row token chunks per expert at the DECODE_MMA token limit
-  float* dense_c;        // [Tmax][dense_n] router logits | shared g | shared u (fp32)
+  float* dense_c;        // [Tmax][dense_n] router logits | pad | shared g | shared u (fp32)
   __nv_bfloat16* h_shared;  // [Tmax][fs] shared-expert h (bf16)
   void* blas_ws;         // cuBLAS workspace
   uint8_t* stage_x;      // host-call staging: x [Tmax][d] bf16
@@ -144,10 +144,10 @@ struct ds4moe_layer {
   CUtensorMap tm_sfb_h1;  // h scale chunks, same
   bool decmma_ready;      // the maps above are encoded
   void* blas;             // cuBLAS handle (router / shared expert), or null
-  __nv_bfloat16* wcat;    // [dense_n][d] router rows | shared gate rows | shared up rows
+  __nv_bfloat16* wcat;    // [dense_n][d] router rows | zero rows to a multiple of 4 | shared gate rows | shared up rows
   __nv_bfloat16* wsd;     // [d][fs] shared down
-  int dense_n;            // rows of wcat (E if a router, + 2 fs if a shared expert)
-  int dense_goff;         // column of the first shared gate output in dense_c
+  int dense_n;            // rows of wcat (dense_goff + 2 fs)
+  int dense_goff;         // column of the first shared gate output in dense_c (E rounded up to 4 with a shared expert)
   bool last_forward_x;    // the most recent forward computed its logits
   cudaEvent_t ev[12];  // kernel timing events (created when timing is enabled)
   bool timing;

@@ -401,8 +401,11 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
       }
     }
     const int fs = cfg->d_ff_shared;
-    L->dense_n = (cfg->has_router ? E : 0) + 2 * fs;
-    L->dense_goff = cfg->has_router ? E : 0;
+    // The shared gate block starts on a multiple of four columns (zero rows
+    // pad the router block), so that the SwiGLU kernel's 16-byte loads of g
+    // and u are aligned for any E.
+    L->dense_goff = cfg->has_router ? (fs > 0 ? (E + 3) / 4 * 4 : E) : 0;
+    L->dense_n = L->dense_goff + 2 * fs;
     if (L->dense_n > 0) {
       constexpr size_t kBlasWs = 32u << 20;
       TRY(alloc(L, &L->wcat, (size_t)L->dense_n * d * 2));
@@ -412,7 +415,8 @@ int ds4moe_layer_create(const ds4moe_config* cfg, const ds4moe_weights* wts, ds4
         TRY(alloc(L, &L->wsd, (size_t)d * fs * 2));
         TRY(alloc(L, &s.h_shared, (size_t)Tm * fs * 2));
       }
-      bool okc = true;
+      const int npad = cfg->has_router ? L->dense_goff - E : 0;  // zero rows after the router's E
+      bool okc = npad == 0 || cudaMemset(L->wcat + (size_t)E * d, 0, (size_t)npad * d * 2) == cudaSuccess;
       if (cfg->has_router)
         okc = okc && cudaMemcpy(L->wcat, wts->router, (size_t)E * d * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
       if (fs > 0) {

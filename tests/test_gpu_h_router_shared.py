@@ -16,6 +16,9 @@ pytestmark = pytest.mark.gpu
 
 TINY = synth.Workload("tiny_rs", 6, 256, 8, 128, 2, 31, 31, "normal")
 MID = synth.Workload("mid_rs", 300, 512, 16, 384, 4, 32, 32, "normal")
+# E = 6: the router block of the dense output is padded to 8 columns so that
+# the shared expert's g and u columns stay 16-byte aligned
+ODD_E = synth.Workload("odd_e_rs", 5, 256, 6, 128, 2, 33, 33, "normal")
 ACT = {"decode": oracle.ACT_EXACT, "decode_mma": oracle.ACT_EXACT, "prefill": oracle.ACT_MXFP8}
 
 
@@ -33,7 +36,7 @@ def _sure_tokens(ref_logits32: np.ndarray, k: int) -> np.ndarray:
 
 
 @pytest.mark.parametrize("path", ["decode", "decode_mma", "prefill"])
-@pytest.mark.parametrize("wl,fs", [(TINY, 128), (MID, 384)], ids=["tiny", "mid"])
+@pytest.mark.parametrize("wl,fs", [(TINY, 128), (MID, 384), (ODD_E, 64)], ids=["tiny", "mid", "odd_e"])
 def test_router_and_shared_expert_from_x(ds4, wl, fs, path):
     W = synth.make_layer_weights(wl, device="cuda")
     D = synth.make_dense_weights(wl, fs, device="cuda")
