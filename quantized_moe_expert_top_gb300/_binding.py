@@ -122,6 +122,45 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def check_tensor(t, name: str, shape: tuple, dtype: torch.dtype, on_cuda: bool) -> None:
+    """Raise ValueError unless t is a contiguous tensor of exactly this shape
+    and dtype, on the current CUDA device (on_cuda) or on the host.  The C ABI
+    takes bare pointers, so a smaller buffer than the call implies would be
+    read or written past its end by the kernels."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if on_cuda:
+        if not t.is_cuda or t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name} must be on the current CUDA device")
+    elif t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+
+
+def expected_weight_shapes(d: int, E: int, f: int, down: str, fs: int = 0) -> dict:
+    """Shapes of the stored weight tensors a layer of these sizes reads."""
+    shapes = {"gate_codes": (E, f, d // 2), "gate_scales": (E, f, d // 32),
+              "up_codes": (E, f, d // 2), "up_scales": (E, f, d // 32),
+              "router": (E, d), "shared_gate": (fs, d), "shared_up": (fs, d), "shared_down": (d, fs)}
+    if down == "q2k":
+        shapes["down_q2k"] = (E, d, f // 256, 84)
+    else:
+        shapes["down_codes"] = (E, d, f // 2)
+        shapes["down_scales"] = (E, d, f // 32)
+    return shapes
+
+
+def _rows(t, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D tensor [T, ...]")
+    return t.shape[0]
+
+
 def _stream_handle(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -131,7 +170,9 @@ def _stream_handle(stream) -> ctypes.c_void_p:
 def route_noalloc(logits: torch.Tensor, k: int, stream=None) -> dict:
     """Routing through ds4moe_route_noalloc (no device allocation inside the
     library; the output tensors are allocated here by torch)."""
-    T, E = logits.shape
+    T = _rows(logits, "logits")
+    E = logits.shape[1]
+    check_tensor(logits, "logits", (T, E), torch.float32, on_cuda=True)
     dev = logits.device
     r = {"topk_idx": torch.empty(max(T, 1), k, dtype=torch.int32, device=dev),
          "topk_w": torch.empty(max(T, 1), k, dtype=torch.float32, device=dev),
@@ -172,10 +213,16 @@ class Layer:
         c.d_ff_shared = weights["shared_gate"].shape[0] if weights.get("shared_gate") is not None else 0
         self.cfg = c
         self.down = down
+        shapes = expected_weight_shapes(d_model, n_experts, d_ff, down, c.d_ff_shared)
+        sizes_ok = d_model % 128 == 0 and d_ff % (256 if down == "q2k" else 128) == 0 and c.d_ff_shared % 32 == 0
         for name, t in weights.items():
+            if t is None:
+                continue
+            if name not in shapes:
+                raise ValueError(f"unknown weight {name}")
             want = torch.bfloat16 if name in _DENSE else torch.uint8
-            if t is not None and (t.dtype != want or not t.is_cuda or not t.is_contiguous()):
-                raise ValueError(f"weight {name} must be a contiguous {want} CUDA tensor")
+            # sizes the library rejects are left to its own status code
+            check_tensor(t, f"weight {name}", shapes[name] if sizes_ok else tuple(t.shape), want, on_cuda=True)
         w = WeightPtrs()
         w.gate_codes = weights["gate_codes"].data_ptr()
         w.gate_scales = weights["gate_scales"].data_ptr()
@@ -201,11 +248,12 @@ class Layer:
     def forward(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
                 stream=None) -> torch.Tensor:
         """Enqueue one forward pass (asynchronous on `stream`)."""
-        T = x.shape[0]
+        T, d, E = _rows(x, "x"), self.cfg.d_model, self.cfg.n_experts
         if out is None:
-            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, device=x.device)
-        assert x.dtype == torch.bfloat16 and logits.dtype == torch.float32 and out.dtype == torch.float32
-        assert x.is_contiguous() and logits.is_contiguous() and out.is_contiguous()
+            out = torch.empty(T, d, dtype=torch.float32, device=x.device)
+        check_tensor(x, "x", (T, d), torch.bfloat16, on_cuda=True)
+        check_tensor(logits, "logits", (T, E), torch.float32, on_cuda=True)
+        check_tensor(out, "out", (T, d), torch.float32, on_cuda=True)
         rc = lib().ds4moe_forward(self._h, _ptr(x), _ptr(logits), _ptr(out), T, _stream_handle(stream))
         if rc != OK:
             raise Ds4moeError(rc, "ds4moe_forward")
@@ -214,10 +262,11 @@ class Layer:
 
     def forward_x(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         """The layer from x alone: router logits, routed experts, shared expert."""
-        T = x.shape[0]
+        T, d = _rows(x, "x"), self.cfg.d_model
         if out is None:
-            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, device=x.device)
-        assert x.dtype == torch.bfloat16 and out.dtype == torch.float32 and x.is_contiguous() and out.is_contiguous()
+            out = torch.empty(T, d, dtype=torch.float32, device=x.device)
+        check_tensor(x, "x", (T, d), torch.bfloat16, on_cuda=True)
+        check_tensor(out, "out", (T, d), torch.float32, on_cuda=True)
         rc = lib().ds4moe_forward_x(self._h, _ptr(x), _ptr(out), T, _stream_handle(stream))
         if rc != OK:
             raise Ds4moeError(rc, "ds4moe_forward_x")
@@ -236,10 +285,12 @@ class Layer:
     def forward_host(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
                      stream=None) -> torch.Tensor:
         """Forward pass on host tensors (copies in, runs, copies out, synchronises)."""
-        T = x.shape[0]
+        T, d, E = _rows(x, "x"), self.cfg.d_model, self.cfg.n_experts
         if out is None:
-            out = torch.empty(T, self.cfg.d_model, dtype=torch.float32, pin_memory=True)
-        assert not x.is_cuda and not logits.is_cuda and not out.is_cuda
+            out = torch.empty(T, d, dtype=torch.float32, pin_memory=True)
+        check_tensor(x, "x", (T, d), torch.bfloat16, on_cuda=False)
+        check_tensor(logits, "logits", (T, E), torch.float32, on_cuda=False)
+        check_tensor(out, "out", (T, d), torch.float32, on_cuda=False)
         rc = lib().ds4moe_forward_host(self._h, _ptr(x), _ptr(logits), _ptr(out), T, _stream_handle(stream))
         if rc != OK:
             raise Ds4moeError(rc, "ds4moe_forward_host")

@@ -92,3 +92,37 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(RuntimeError, match="is missing"):
         B.lib()
+
+
+def test_binding_checks_tensor_shapes_before_the_call():
+    """The C ABI takes bare pointers, so the binding checks every tensor's
+    shape, dtype, contiguity and device before handing its pointer over."""
+    import pytest
+    import torch
+    import quantized_moe_expert_top_gb300._binding as B
+    ok = torch.zeros(4, 256, dtype=torch.bfloat16)
+    B.check_tensor(ok, "x", (4, 256), torch.bfloat16, on_cuda=False)
+    bad = [
+        (torch.zeros(4, 256, dtype=torch.float32), "must be torch.bfloat16"),       # dtype
+        (torch.zeros(3, 256, dtype=torch.bfloat16), "must have shape"),             # too few rows
+        (torch.zeros(4, 128, dtype=torch.bfloat16), "must have shape"),             # too few columns
+        (torch.zeros(256, 4, dtype=torch.bfloat16).t(), "must be contiguous"),     # strided view
+        ([0.0] * 1024, "must be a torch.Tensor"),
+    ]
+    for t, msg in bad:
+        with pytest.raises(ValueError, match=msg):
+            B.check_tensor(t, "x", (4, 256), torch.bfloat16, on_cuda=False)
+    with pytest.raises(ValueError, match="current CUDA device"):  # a host tensor where device memory is needed
+        B.check_tensor(ok, "x", (4, 256), torch.bfloat16, on_cuda=True)
+    with pytest.raises(ValueError, match="2-D"):
+        B._rows(torch.zeros(1024, dtype=torch.bfloat16), "x")
+
+
+def test_expected_weight_shapes_match_the_generators():
+    import synth
+    import quantized_moe_expert_top_gb300._binding as B
+    for down in ("mxfp4", "q2k"):
+        wl = synth.Workload("shapes_" + down, 2, 256, 3, 256, 2, 1, 1, "normal", down)
+        W = {**synth.make_layer_weights(wl), **synth.make_dense_weights(wl, 64)}
+        want = B.expected_weight_shapes(wl.d, wl.E, wl.f, down, 64)
+        assert {n: tuple(t.shape) for n, t in W.items()} == {n: want[n] for n in W}
