@@ -126,3 +126,41 @@ def test_expected_weight_shapes_match_the_generators():
         W = {**synth.make_layer_weights(wl), **synth.make_dense_weights(wl, 64)}
         want = B.expected_weight_shapes(wl.d, wl.E, wl.f, down, 64)
         assert {n: tuple(t.shape) for n, t in W.items()} == {n: want[n] for n in W}
+
+
+def test_layer_calls_check_before_reaching_the_library(monkeypatch):
+    """Layer.forward_host / forward hand their pointers to the library only
+    after the checks pass (a fake library records the calls; no GPU)."""
+    import pytest
+    import torch
+    import quantized_moe_expert_top_gb300._binding as B
+    calls = []
+
+    class FakeLib:
+        def ds4moe_forward_host(self, *a):
+            calls.append("forward_host")
+            return B.OK
+
+        def ds4moe_forward(self, *a):
+            calls.append("forward")
+            return B.OK
+
+    class FakeStream:
+        cuda_stream = 0
+
+    monkeypatch.setattr(B, "lib", lambda: FakeLib())
+    layer = object.__new__(B.Layer)
+    layer._h = None
+    layer.cfg = B.Config()
+    layer.cfg.d_model, layer.cfg.n_experts = 256, 8
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    lg = torch.zeros(4, 8, dtype=torch.float32)
+    out = torch.zeros(4, 256, dtype=torch.float32)
+    layer.forward_host(x, lg, out, stream=FakeStream())
+    assert calls == ["forward_host"]
+    for args in ((x, torch.zeros(3, 8), out), (x, lg, torch.zeros(4, 128)), (x.float(), lg, out)):
+        with pytest.raises(ValueError):
+            layer.forward_host(*args, stream=FakeStream())
+    with pytest.raises(ValueError, match="current CUDA device"):
+        layer.forward(x, lg, out, stream=FakeStream())
+    assert calls == ["forward_host"]
