@@ -104,3 +104,16 @@ def test_dominant_roofline_picks_the_slowest_kernel_and_its_bound():
     assert r["achieved"] == pytest.approx(flops / 0.5e-3 / 1e12)
     assert r["hbm_frac"] == pytest.approx(acc["gemm_gateup_bytes"] / 0.5e-3 / 1e9 / 6000.0)
     assert bench.dominant_roofline({}, acc, "prefill", peaks, 4000.0, 12000.0) is None
+
+
+def test_config_states_the_l2_rule_of_the_timed_steps():
+    """Both arms print config_of(...) unchanged; it says how L2 is kept out
+    of the timing, by the same rule the timed loop follows."""
+    import synth
+    pre, dec = synth.WORKLOADS["prefill"], synth.WORKLOADS["decode1"]
+    assert not bench.flushes_l2(pre) and bench.flushes_l2(dec)
+    c = bench.config_of(pre, 1)
+    # 256 experts x (gate + up MXFP4 [2048 x 4096] + down MXFP4 [4096 x 2048]) = 3.42 GB > the 129 MB L2
+    assert c["l2"].startswith("inputs larger than L2") and "3.42 GB" in c["l2"]
+    assert bench.config_of(dec, 1)["l2"].startswith("flushed")
+    assert c["workload"].startswith("prefill: T=4096 d=4096 E=256 f=2048 top_k=8")
