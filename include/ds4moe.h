@@ -44,7 +44,10 @@
  *
  * Conventions for every call:
  *   - Return value: DS4MOE_OK (0) or a negative DS4MOE_ERR_* code.  A call
- *     that returns an error has enqueued no GPU work.
+ *     that returns INVALID_ARG, UNSUPPORTED or TOO_MANY_TOKENS has enqueued
+ *     no GPU work (those checks run on the host first); after DS4MOE_ERR_CUDA
+ *     (a launch or copy failed) the work enqueued before the failing step may
+ *     still run, and the call's outputs are invalid.
  *   - "device pointer" = global memory of the layer's device; "host pointer"
  *     = CPU memory (pinned memory gives the fastest copies).
  *   - Every device pointer must be 16-byte aligned.
@@ -162,9 +165,9 @@ int ds4moe_layer_create(const ds4moe_config *cfg, const ds4moe_weights *weights,
  *   T       0..max_tokens (T = 0 enqueues nothing)
  * x, logits and out stay owned by the caller and must stay valid until the
  * stream work completes; out must not overlap x or logits (INVALID_ARG).
- * Errors (checked on the host before anything is enqueued): INVALID_ARG,
- * TOO_MANY_TOKENS, CUDA (a launch failed).  Device-side timeouts surface
- * later through ds4moe_get_status. */
+ * Errors: INVALID_ARG, UNSUPPORTED and TOO_MANY_TOKENS (checked on the host
+ * before anything is enqueued), CUDA (a launch failed).  Device-side timeouts
+ * surface later through ds4moe_get_status. */
 int ds4moe_forward(ds4moe_layer *layer, const void *x, const float *logits, float *out,
                    int32_t T, ds4moe_stream_t stream);
 
